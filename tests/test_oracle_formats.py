@@ -1,0 +1,112 @@
+"""Pins for the oracle's number formats: bf16 and E4M3 rounding, E4M3 decoding, row quantiser."""
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bits_f32(x):
+    return np.asarray(x, np.float32).view(np.uint32)
+
+
+def test_bf16_round_matches_torch_on_float32_inputs(orc):
+    rng = np.random.default_rng(1)
+    # random bit patterns over a wide exponent range, plus exact ties (low 16 bits = 0x8000)
+    u = rng.integers(0, 2**32, 400_000, dtype=np.uint64).astype(np.uint32)
+    u = u[((u >> 23) & 0xFF) < 0xFF]                       # finite only
+    ties = (u & 0xFFFF0000) | 0x8000
+    u = np.concatenate([u, ties]).astype(np.uint32)
+    x = u.view(np.float32)
+    ref = torch.from_numpy(x.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = orc.bf16_round(x.astype(np.float64))
+    assert np.array_equal(got, ref)
+
+
+def test_bf16_round_single_rounding_from_double(orc):
+    # 1 + 2^-8 + 2^-30 lies just above the midpoint between 1 and 1 + 2^-7: rounding the double
+    # once gives 1 + 2^-7 (0x3F81); rounding through float32 first would tie to 1.0 (0x3F80).
+    x = 1.0 + 2.0**-8 + 2.0**-30
+    assert int(orc.bf16_round([x])[0]) == 0x3F81
+    assert int(orc.bf16_round([-x])[0]) == 0xBF81
+    assert int(orc.bf16_round([1.0 + 2.0**-8])[0]) == 0x3F80     # exact tie -> even
+    assert int(orc.bf16_round([1.0 + 3 * 2.0**-8])[0]) == 0x3F82  # tie -> even (up)
+
+
+def test_e4m3_published_encodings(orc):
+    rows = []
+    with open(os.path.join(GOLDEN, "e4m3_kat.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                a, b = line.split()
+                rows.append((int(a, 16), float(b)))
+    codes = np.array([a for a, _ in rows], np.uint8)
+    vals = np.array([b for _, b in rows], np.float64)
+    dec = orc.e4m3_value(codes)
+    assert np.array_equal(dec, vals)
+    assert np.array_equal(np.signbit(dec), np.signbit(vals))
+    enc = orc.e4m3_round(vals.astype(np.float32))
+    assert np.array_equal(enc, codes)
+    assert np.isnan(orc.e4m3_value(np.array([0x7F, 0xFF], np.uint8))).all()
+
+
+def test_e4m3_decode_all_codes_matches_torch(orc):
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = orc.e4m3_value(codes)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_e4m3_round_exhaustive_over_bf16_inputs(orc):
+    # every bf16 value with magnitude <= 448 (where no saturation can occur) against torch
+    b = np.arange(1 << 16, dtype=np.uint32)
+    x = (b << 16).view(np.float32)
+    keep = np.isfinite(x) & (np.abs(x) <= 448.0)
+    x = x[keep]
+    ref = torch.from_numpy(x.copy()).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = orc.e4m3_round(x)
+    assert np.array_equal(got, ref)
+
+
+def test_e4m3_satfinite(orc):
+    x = np.array([464.0, 465.0, 480.0, 1e9, np.inf, -np.inf, -500.0, 447.0], np.float32)
+    got = orc.e4m3_round(x)
+    # 464 is the midpoint between 448 (mantissa 110) and 480 (not finite): ties-to-even keeps 448
+    assert list(got[:7]) == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE]
+    assert got[7] == 0x7E      # 447 rounds to 448 (spacing 32 above 256)
+    assert np.isnan(orc.e4m3_value(orc.e4m3_round(np.array([np.nan], np.float32)))).all()
+
+
+def _bf16(vals):
+    return (np.asarray(vals, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_quant_rows_hand_example(orc):
+    h = _bf16([[1.0, -2.0, 0.5, 0.0], [0.0, 0.0, 0.0, 0.0]]).reshape(-1)
+    q, sc = orc.quant_rows_e4m3(h, 2, 4)
+    # amax = 2, inv = 224: products 224, -448, 112, 0
+    assert list(q[:4]) == [0x76, 0xFE, 0x6E, 0x00]
+    assert sc[0] == np.float32(2.0) / np.float32(448.0)
+    assert list(q[4:]) == [0, 0, 0, 0] and sc[1] == np.float32(1.0)
+
+
+def test_quant_rows_error_bound_and_amax(orc):
+    rng = np.random.default_rng(3)
+    rows, d = 64, 96
+    x = rng.standard_normal(rows * d).astype(np.float32) * np.float32(3.0)
+    hb = _bf16(x)
+    q, sc = orc.quant_rows_e4m3(hb, rows, d)
+    hv = (hb.astype(np.uint32) << 16).view(np.float32).astype(np.float64).reshape(rows, d)
+    deq = orc.e4m3_value(q).reshape(rows, d) * sc.astype(np.float64)[:, None]
+    amax = np.abs(hv).max(axis=1)
+    # the row maximum maps to code magnitude 448 (0x7E / 0xFE)
+    for r in range(rows):
+        k = int(np.argmax(np.abs(hv[r])))
+        assert (q[r * d + k] & 0x7F) == 0x7E
+    # relative error of a normal E4M3 value is at most 2^-4; subnormal absolute error 2^-10*scale
+    err = np.abs(deq - hv)
+    bound = np.maximum(np.abs(hv) * 2.0**-4, 2.0**-10 * sc.astype(np.float64)[:, None]) * 1.0001
+    assert (err <= bound + 1e-12 * amax[:, None]).all()
