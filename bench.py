@@ -1,0 +1,445 @@
+"""Benchmark of the canvas pass on B300: canvas passes/s (and slots/s) and % of roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+One step = one pass of the whole hot path over one batch of synthetic inputs: the vocabulary
+head contraction with fused softmax statistics, the cross-group merge, the confidence top-K
+keep, the counter-hash re-randomisation and the stop test (dg_canvas_step with a device stop
+state). Loop configurations time one full dg_canvas_loop per step and count the passes it ran.
+The default workload is one 256-slot canvas over a 262144-token bf16 head with d = 2816.
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU (the path has no
+exchange step); the timed region is bracketed by barriers and the max over ranks is reported.
+Prints ONE JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_CONFIG = "pass_bf16_v262144_d2816"
+L2_BYTES = 126 * 1024 * 1024
+
+
+# ---------------------------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws: int, backend: str):
+    if ws > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(ws: int):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(units_per_rank: float, seconds_max: float, ws: int) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    return units_per_rank * ws / seconds_max
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------------------------
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}",
+                                          f"--query-gpu={CLOCK_QUERY}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) >= 9:
+                rows.append(p)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(pw) if pw else None}
+
+
+# ---------------------------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------------------------
+def to_dev_bf16(bits, shape):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).reshape(shape).cuda()
+
+
+def algorithmic(cfg):
+    """FLOPs and algorithmic bytes of one pass (operands read once, O(R) outputs)."""
+    eb = {"f32": 4, "bf16": 2, "e4m3": 1}[cfg.precision]
+    flops = 2.0 * cfg.R * cfg.V * cfg.d
+    byts = cfg.V * cfg.d * eb + cfg.R * cfg.d * eb + cfg.R * (4 + 4 + 4 + 1 + 4)
+    if cfg.precision == "e4m3":
+        byts += cfg.V * 4 + cfg.R * 4
+    return flops, byts
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+def run_ours(args, cfg, ws_, rank):
+    import uniform_state_denoising_vocab_b300 as dg
+    from workloads import make_loop_inputs, make_pass_inputs
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    flops, byts = algorithmic(cfg)
+    R, d, V = cfg.R, cfg.d, cfg.V
+    launches_per_step = 2 + (1 if cfg.precision == "e4m3" else 0)
+
+    if cfg.mode == "pass":
+        x = make_pass_inputs(cfg)
+        if cfg.precision == "f32":
+            h = torch.from_numpy(x["h"]).view(R, d).cuda()
+            w = torch.from_numpy(x["w"]).view(V, d).cuda()
+            wsc = None
+        elif cfg.precision == "bf16":
+            h, w, wsc = to_dev_bf16(x["h"], (R, d)), to_dev_bf16(x["w"], (V, d)), None
+        else:
+            h = to_dev_bf16(x["h"], (R, d))
+            w = torch.from_numpy(x["w"]).view(V, d).cuda()
+            wsc = torch.from_numpy(x["w_scale"]).cuda()
+        del x["w"]
+        canvas = torch.from_numpy(x["canvas"]).cuda()
+        canvas_out = torch.empty_like(canvas)
+        state = dg.new_state(cfg.B, dev)
+        rule = dg.StopRule(max_passes=1 << 30, entropy_threshold=0.0, stable_passes=1 << 30,
+                           stop_mode=dg.STOP_OR)
+        desc = dg.make_desc(h, w, B=cfg.B, S=cfg.S, w_scale=wsc)
+        wsb = torch.empty(dg.dg_workspace_bytes(desc) + 256, dtype=torch.uint8, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        outs = {"argmax": torch.empty(R, dtype=torch.int32, device=dev),
+                "conf": torch.empty(R, device=dev), "entropy": torch.empty(R, device=dev),
+                "kept": torch.empty(R, dtype=torch.uint8, device=dev),
+                "mean_entropy": torch.empty(cfg.B, device=dev)}
+        import ctypes as C
+        L = dg.lib()
+        P = lambda t: C.c_void_p(t.data_ptr()) if t is not None else None
+        sh = C.c_void_p(stream.cuda_stream)
+        rref = C.byref(rule)
+        dref = C.byref(desc)
+
+        def step(i, cin, cout):
+            rc = L.dg_canvas_step(dref, P(cin), P(cout), cfg.keep_k, C.c_uint64(cfg.seed),
+                                  C.c_uint32(i), P(outs["argmax"]), P(outs["conf"]),
+                                  P(outs["entropy"]), P(outs["kept"]), P(outs["mean_entropy"]),
+                                  P(state), rref, P(wsb), wsb.numel(), P(status), sh)
+            if rc != 0:
+                raise RuntimeError(dg.dg_status_string(rc))
+
+        for i in range(args.warmup):
+            step(i, canvas, canvas_out)
+        torch.cuda.synchronize()
+        # device-resident timed region
+        barrier(ws_)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        heads = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)]
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            ev0.record(stream)
+            for i in range(args.steps):
+                dg.dg_profile_next_head(*heads[i])
+                step(args.warmup + i, canvas if i % 2 == 0 else canvas_out,
+                     canvas_out if i % 2 == 0 else canvas)
+            ev1.record(stream)
+            torch.cuda.synchronize()
+        barrier(ws_)
+        t_ms = ev0.elapsed_time(ev1)
+        head_ms = [a.elapsed_time(b) for a, b in heads]
+        clocks = clk.summary()
+        st = int(status.item())
+        # end-to-end through the public API with host buffers: pinned h and canvas in, the new
+        # canvas and mean entropy out, every step
+        h_host = h.cpu().pin_memory()
+        c_host = canvas.cpu().pin_memory()
+        c_back = torch.empty_like(c_host).pin_memory()
+        m_back = torch.empty(cfg.B, dtype=torch.float32).pin_memory()
+        e_steps = max(10, args.steps // 4)
+        barrier(ws_)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(e_steps):
+            h.copy_(h_host, non_blocking=True)
+            canvas.copy_(c_host, non_blocking=True)
+            step(i, canvas, canvas_out)
+            c_back.copy_(canvas_out, non_blocking=True)
+            m_back.copy_(outs["mean_entropy"], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws_)
+        e_ms = e1.elapsed_time(e0) * -1.0 if False else e0.elapsed_time(e1)
+        h2d = h_host.numel() * h_host.element_size() + c_host.numel() * 4
+        d2h = c_back.numel() * 4 + m_back.numel() * 4
+        units = cfg.B * args.steps          # canvas passes
+        e_units = cfg.B * e_steps
+        return {"t_s": t_ms / 1e3, "units": units, "head_ms": head_ms, "clocks": clocks,
+                "status": st, "e2e_t_s": e_ms / 1e3, "e2e_units": e_units, "h2d": h2d, "d2h": d2h,
+                "launches": launches_per_step * args.steps, "flops": flops, "bytes": byts}
+
+    # loop mode: one step = one whole loop (denoiser + quantiser + head + select per pass)
+    x = make_loop_inputs(cfg)
+    if cfg.precision == "bf16":
+        w, wsc = to_dev_bf16(x["w"], (V, d)), None
+    else:
+        w = torch.from_numpy(x["w"]).view(V, d).cuda()
+        wsc = torch.from_numpy(x["w_scale"]).cuda()
+    y = torch.from_numpy(x["y"]).cuda()
+    canvas = torch.empty(R, dtype=torch.int32, device=dev)
+    hbuf = torch.empty(R, d, dtype=torch.bfloat16, device=dev)
+    state = dg.new_state(cfg.B, dev)
+    desc = dg.make_desc(hbuf, w, B=cfg.B, S=cfg.S, w_scale=wsc)
+    wsb = torch.empty(dg.dg_workspace_bytes(desc) + 256, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    kw = dict(B=cfg.B, S=cfg.S, theta=cfg.theta, y=y, h_buffer=hbuf, w_scale=wsc,
+              keep_k0=cfg.keep_k, seed=cfg.seed, max_passes=cfg.max_passes,
+              stable_passes=cfg.stable_passes, n_content=cfg.n_content, s_content=cfg.s_content,
+              s_pad=cfg.s_pad, state=state, workspace=wsb, status=status)
+    for _ in range(args.warmup):
+        dg.dg_canvas_loop(w, canvas, **kw)
+    torch.cuda.synchronize()
+    passes_per_loop = int(dg.state_fields(state)["passes"].sum())
+    barrier(ws_)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            dg.dg_canvas_loop(w, canvas, **kw)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws_)
+    t_ms = ev0.elapsed_time(ev1)
+    # end-to-end: targets in, final canvas + state out, every loop
+    y_host = y.cpu().pin_memory()
+    c_back = torch.empty(R, dtype=torch.int32).pin_memory()
+    s_back = torch.empty_like(state, device="cpu").pin_memory()
+    e_steps = max(3, args.steps // 4)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        y.copy_(y_host, non_blocking=True)
+        dg.dg_canvas_loop(w, canvas, **kw)
+        c_back.copy_(canvas, non_blocking=True)
+        s_back.copy_(state, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1)
+    per_pass = 3 + (1 if cfg.precision == "e4m3" else 0)
+    return {"t_s": t_ms / 1e3, "units": passes_per_loop * args.steps, "head_ms": None,
+            "clocks": clk.summary(), "status": int(status.item()), "e2e_t_s": e_ms / 1e3,
+            "e2e_units": passes_per_loop * e_steps, "h2d": y_host.numel() * 4,
+            "d2h": c_back.numel() * 4 + s_back.numel() * 4,
+            "launches": args.steps * (1 + per_pass * passes_per_loop),
+            "flops": flops, "bytes": byts, "passes_per_loop": passes_per_loop}
+
+
+# ---------------------------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------------------------
+def oracle_sample(cfg, target_s: float = 15.0):
+    """Time the oracle on a bounded sample of the workload: a few slot rows against the full
+    vocabulary (statistics), plus the keep/re-randomise step for the whole canvas, and scale to
+    canvas passes/s by rows. Returns (passes_per_s, sample description, cores)."""
+    import oracle
+    from workloads.gen import make_head, normal_f32, f32_to_bf16_bits, TAG_H
+    oracle.build()
+    V, d, R = cfg.V, cfg.d, cfg.R
+    head = make_head(cfg)
+    w = head["w"]
+    wsc = head["w_scale"]
+    rows = 1
+    h = normal_f32(R * d, cfg.seed, TAG_H)
+    if cfg.precision != "f32":
+        h = f32_to_bf16_bits(h)
+    hs = None
+    if cfg.precision == "e4m3":
+        h, hs = oracle.quant_rows_e4m3(h, R, d)
+    # calibrate with one row, then size the sample to roughly target_s seconds
+    t0 = time.perf_counter()
+    oracle.head_stats(R, d, V, cfg.precision, h, w, h_scale=hs, w_scale=wsc, rows=np.arange(rows))
+    t1 = time.perf_counter() - t0
+    rows = int(max(1, min(R, target_s / max(t1, 1e-6))))
+    t0 = time.perf_counter()
+    st = oracle.head_stats(R, d, V, cfg.precision, h, w, h_scale=hs, w_scale=wsc,
+                           rows=np.arange(rows))
+    t_stats = time.perf_counter() - t0
+    # the per-canvas step on the full canvas (cheap): reuse the sampled rows' stats cyclically
+    idx = np.arange(R) % rows
+    t0 = time.perf_counter()
+    oracle.select(cfg.B, cfg.S, V, st["argmax"][idx], st["conf"][idx], st["entropy"][idx],
+                  cfg.keep_k, cfg.seed, 0)
+    t_sel = time.perf_counter() - t0
+    per_pass = t_stats * (R / rows) + t_sel
+    desc = (f"{rows} of {R} slot rows x full vocabulary {V} x d={d} (statistics), plus the "
+            f"keep/re-randomise step on all {R} rows; scaled by rows to one pass")
+    return 1.0 / per_pass, desc, oracle.num_threads(), per_pass
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from workloads import CONFIGS
+    cfg = CONFIGS[args.config]
+    ws_, rank, local = dist_env()
+    metric = "canvas passes/s (256 slots x 262K vocab, d=2816) and % of roofline, 1 B300"
+    workload = {"workload": cfg.name, "canvases": cfg.B, "slots": cfg.S, "vocab": cfg.V,
+                "hidden": cfg.d, "precision": cfg.precision, "mode": cfg.mode,
+                "keep_k": cfg.keep_k, "seed": cfg.seed,
+                "l2": "inputs larger than L2 (head %.2f GB)" % (cfg.V * cfg.d * {"f32": 4, "bf16": 2, "e4m3": 1}[cfg.precision] / 1e9)
+                if cfg.V * cfg.d > L2_BYTES else "L2-resident head, latency-bound"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        times = []
+        for _ in range(args.warmup):
+            pass
+        vals = []
+        desc = ""
+        cores = 0
+        for _ in range(max(1, args.steps if args.steps <= 3 else 3)):
+            v, desc, cores, per = oracle_sample(cfg, target_s=5.0)
+            vals.append(v)
+            times.append(per)
+        v = statistics.median(vals)
+        line = {"impl": "reference", "metric": metric, "value": v, "unit": "canvas passes/s",
+                "n_gpus": args.gpus, "steps": len(vals), "warmup": 0,
+                "ms_per_step": statistics.median(times) * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": workload,
+                "cpu_baseline": {"value": v, "unit": "canvas passes/s", "cores": cores,
+                                 "kind": "oracle", "sample": desc},
+                "e2e": {"value": v, "unit": "canvas passes/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    init_dist(ws_, "nccl")
+    torch.cuda.set_device(local)
+    r = run_ours(args, cfg, ws_, rank)
+    t_max = max_over_ranks(r["t_s"], ws_, torch.device("cuda", local))
+    e_max = max_over_ranks(r["e2e_t_s"], ws_, torch.device("cuda", local))
+    if rank != 0:
+        if ws_ > 1:
+            torch.distributed.destroy_process_group()
+        return
+    value = aggregate(r["units"], t_max, ws_)
+    e2e = aggregate(r["e2e_units"], e_max, ws_)
+    peaks, peak_kind = load_peaks()
+    line = {"metric": metric, "value": value, "unit": "canvas passes/s", "n_gpus": ws_,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": {"f32": "f32", "bf16": "bf16", "e4m3": "e4m3"}[cfg.precision],
+            "data": "synthetic (seeded N(0,1) hidden states, N(0,1/d) head)",
+            "config": workload, "slots_per_s": value * cfg.S,
+            "e2e": {"value": e2e, "unit": "canvas passes/s", "h2d_bytes_per_step": r["h2d"],
+                    "d2h_bytes_per_step": r["d2h"]},
+            "gpu_launches": r["launches"], "clocks": r["clocks"], "device_status": r["status"]}
+    if r["head_ms"]:
+        head_s = statistics.mean(r["head_ms"]) / 1e3
+        t_mem = r["bytes"] / (peaks["hbm_gbs"] * 1e9)
+        tens_peak = peaks["bf16_tflops"] * (2.0 if cfg.precision == "e4m3" else 1.0)
+        t_flop = r["flops"] / (tens_peak * 1e12)
+        bound = "hbm" if t_mem >= t_flop else "tensor"
+        if bound == "hbm":
+            achieved = r["bytes"] / head_s / 1e9
+            line["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                                "traffic": None, "peak_source": peak_kind + " (burst copy)"}
+        else:
+            achieved = r["flops"] / head_s / 1e12
+            line["roofline"] = {"bound": "tensor", "achieved": achieved, "peak": tens_peak,
+                                "unit": "TFLOP/s", "frac": achieved / tens_peak, "traffic": None,
+                                "peak_source": peak_kind + " (burst bf16 cuBLAS"
+                                + (" x2 nominal fp8/bf16 ratio)" if cfg.precision == "e4m3" else ")")}
+        line["roofline"]["kernel"] = "head_tc_kernel" if cfg.precision != "f32" else "head_simt_kernel"
+        line["roofline"]["kernel_us"] = head_s * 1e6
+        line["roofline"]["step_roof_frac"] = max(t_mem, t_flop) / (t_max / args.steps)
+        line["roofline"]["tensor_frac"] = (r["flops"] / head_s / 1e12) / tens_peak
+    if not args.no_cpu_baseline and ws_ == 1:
+        v, desc, cores, _ = oracle_sample(cfg)
+        line["cpu_baseline"] = {"value": v, "unit": "canvas passes/s", "cores": cores,
+                                "kind": "oracle", "sample": desc}
+    print(json.dumps(line))
+    if ws_ > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

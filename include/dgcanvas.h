@@ -1,0 +1,233 @@
+/*
+ * dgcanvas.h -- C ABI of libdgcanvas.so: the per-pass canvas update of a uniform-state block
+ * text-diffusion sampler, on one B300 (sm_103a).
+ *
+ * The method (as the pages describe it):
+ *   - A canvas is a fixed block of 256 token slots ("DiffusionGemma 26B: How Google's Text
+ *     Diffusion Model Generates Tokens in Parallel" (dev.to), "Architecture Details": canvas
+ *     length 256, vocabulary 262K).
+ *   - Uniform-state diffusion: the canvas starts from random vocabulary tokens and any slot can
+ *     be revised later. Each pass predicts every slot at once, keeps the slots it is most
+ *     confident about and re-randomises the rest ("When to use a diffusion LLM"
+ *     (devengoratela.com), "How block diffusion works").
+ *   - The loop stops when the average canvas entropy drops below a threshold or the tokens are
+ *     stable across two consecutive steps, after at most 48 steps (dev.to page, "How Diffusion
+ *     Changes the Equation"); the average runs over all 256 slots including padding
+ *     (devengoratela.com page, "How block diffusion works").
+ *
+ * Readings fixed by this library where the pages are silent:
+ *   - confidence of a slot = max_n p_n of its softmax over the vocabulary; entropy in nats;
+ *   - keep the K most confident slots of each canvas, ties to the lower slot index; argmax ties
+ *     to the lower vocabulary index;
+ *   - re-randomised token of row r = b*S + slot at pass p: key(seed, p, r) mod V with
+ *     key(seed, p, r) = sm64(sm64(sm64(seed) ^ p) ^ r) and sm64 one SplitMix64 output
+ *     (Steele, Lea & Flood, OOPSLA 2014); the initial random canvas uses p = 0xFFFFFFFF;
+ *   - the stop rules are OR-combined by default (DG_STOP_AND requires entropy AND stability),
+ *     "stable" = the update left the whole canvas unchanged for `stable_passes` consecutive
+ *     passes, the entropy test is strict (mean H < threshold).
+ *
+ * Conventions for every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller (for example PyTorch tensors),
+ *     16-byte aligned. The library allocates no device memory on the step path: the caller
+ *     passes a workspace of at least dg_workspace_bytes() bytes, 256-byte aligned.
+ *   - `stream` is the caller's cudaStream_t (NULL = legacy default stream). Calls only enqueue
+ *     work and never synchronise; results are valid once the stream reaches them.
+ *   - Return value: DG_OK or a negative DG_ERR_* code; on error nothing was enqueued (except
+ *     DG_ERR_CUDA, which reports a failed launch). Data problems found on the device (token ids
+ *     outside [0, V), non-finite logits, a bounded wait that ran out) do not trap: they set
+ *     sticky DG_ST_* bits in the caller's device `status` word (which the caller zeroes), and
+ *     the affected outputs are unspecified.
+ */
+#ifndef DGCANVAS_H
+#define DGCANVAS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DG_API __attribute__((visibility("default")))
+#else
+#define DG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dg_stream_t; /* identical to cudaStream_t */
+
+typedef enum { DG_F32 = 0, DG_BF16 = 1, DG_E4M3 = 2 } dg_dtype;
+
+enum {
+    DG_OK = 0,
+    DG_ERR_INVALID_ARG = -1,  /* null/negative/inconsistent argument */
+    DG_ERR_ALIGNMENT = -2,    /* pointer not 16-byte aligned, or d*elem_size % 16 != 0 */
+    DG_ERR_UNSUPPORTED = -3,  /* not sm_103, dtype pair not supported, S > 1024, V >= 2^31 */
+    DG_ERR_WORKSPACE = -4,    /* workspace NULL, misaligned or smaller than required */
+    DG_ERR_CUDA = -5          /* a CUDA runtime call or kernel launch failed */
+};
+
+/* Sticky device status bits. */
+enum {
+    DG_ST_BAD_TOKEN = 1u,  /* an input canvas or target id was outside [0, V) */
+    DG_ST_NONFINITE = 2u,  /* a non-finite logit or hidden value reached the statistics */
+    DG_ST_TIMEOUT = 4u     /* a bounded on-device wait ran out; that kernel returned early */
+};
+
+/* Stop reasons (bitmask of every rule true at the stopping pass). */
+enum { DG_REASON_ENTROPY = 1, DG_REASON_STABLE = 2, DG_REASON_CAP = 4 };
+enum { DG_STOP_OR = 0, DG_STOP_AND = 1 };
+
+/*
+ * The vocabulary head and the hidden states of one batch of canvases.
+ *   h       [B*S, d] row-major, row r = b*S + slot. dtype h_dtype.
+ *   h_scale [B*S] fp32 per-row scales when h_dtype == DG_E4M3, else NULL.
+ *   w       [V, d] row-major vocabulary head. dtype w_dtype.
+ *   w_scale [V] fp32 per-row scales when w_dtype == DG_E4M3, else NULL.
+ * logits l[r, n] = inv_temp * sum_k h[r,k] * w[n,k] (times h_scale[r] * w_scale[n] for E4M3),
+ * accumulated in fp32 and never stored.
+ * Supported (h_dtype, w_dtype): (F32, F32) on CUDA cores; (BF16, BF16) and (E4M3, E4M3) on the
+ * tensor cores; (BF16, E4M3) quantises h per row to E4M3 first (absmax scaling:
+ * scale = amax/448, q = e4m3_rn_satfinite(h * (448/amax)), all in fp32; amax = 0 gives scale 1).
+ * Limits: 1 <= S <= 1024, B >= 1, 1 <= V < 2^31, d >= 1 with d*elem_size(dtype) % 16 == 0.
+ */
+typedef struct {
+    int32_t B, S, d, V;
+    int32_t h_dtype, w_dtype; /* dg_dtype */
+    const void* h;
+    const float* h_scale;
+    const void* w;
+    const float* w_scale;
+    float inv_temp;           /* 1.0f = untempered statistics */
+} dg_head_desc;
+
+/* Per-canvas loop state in device memory (32 bytes per canvas). */
+typedef struct {
+    int32_t passes;       /* passes completed when the canvas stopped, else 0 */
+    int32_t reason;       /* DG_REASON_* bitmask at the stopping pass, else 0 */
+    int32_t stable;       /* consecutive passes that left the canvas unchanged */
+    int32_t done;         /* 1 once stopped: later passes leave the canvas frozen */
+    float mean_entropy;   /* mean slot entropy (nats) of the last pass that ran */
+    int32_t last_pass;    /* index of the last pass that updated this canvas, -1 before */
+    int32_t reserved[2];
+} dg_canvas_state;
+
+/* Stop rule parameters for dg_canvas_step with a state, and for dg_canvas_loop. */
+typedef struct {
+    int32_t max_passes;        /* pass cap (48 in the pages) */
+    float entropy_threshold;   /* stop when mean H < threshold (nats) */
+    int32_t stable_passes;     /* stop when unchanged for this many consecutive passes (2) */
+    int32_t stop_mode;         /* DG_STOP_OR or DG_STOP_AND */
+} dg_stop_rule;
+
+/* Bytes of workspace a call with this descriptor needs (same for stats/step/loop). */
+DG_API int dg_workspace_bytes(const dg_head_desc* desc, size_t* bytes);
+
+/*
+ * Softmax statistics of every slot, without storing logits:
+ *   argmax[r] (int32), conf[r] = max_n p_n (fp32), entropy[r] = -sum_n p_n ln p_n (fp32, nats),
+ *   mean_entropy[b] = mean over the S slots of canvas b (fp32, fixed summation order).
+ * Any output pointer may be NULL. status: device uint32 (sticky DG_ST_* bits), may be NULL.
+ */
+DG_API int dg_canvas_stats(const dg_head_desc* desc, int32_t* argmax, float* conf, float* entropy,
+                    float* mean_entropy, void* workspace, size_t workspace_bytes,
+                    uint32_t* status, dg_stream_t stream);
+
+/*
+ * One canvas pass: statistics, keep the K = min(keep_k, S) most confident slots of each canvas
+ * at their argmax, re-draw the others as key(seed, pass, r) mod V, write canvas_out [B*S].
+ * canvas_in == canvas_out is allowed. kept [B*S] (uint8 0/1) and the statistics outputs may be
+ * NULL. If `state` (device, [B]) and `rule` (host) are given, the pass also applies the stop
+ * test: it updates stable/done/passes/reason, and canvases already done are left unchanged
+ * (copied to canvas_out). rule may only be NULL when state is NULL.
+ */
+DG_API int dg_canvas_step(const dg_head_desc* desc, const int32_t* canvas_in, int32_t* canvas_out,
+                   int32_t keep_k, uint64_t seed, uint32_t pass, int32_t* argmax, float* conf,
+                   float* entropy, uint8_t* kept, float* mean_entropy, dg_canvas_state* state,
+                   const dg_stop_rule* rule, void* workspace, size_t workspace_bytes,
+                   uint32_t* status, dg_stream_t stream);
+
+/*
+ * Denoiser hook of the loop: enqueue, on `stream`, work that reads the canvas (device int32
+ * [B*S]) and the pass index (device int32 scalar) and writes the hidden states h_out (device,
+ * [B*S, d] in the descriptor's h_dtype; BF16 when the head is E4M3 and h is quantised by the
+ * library). It must be stream-ordered and capturable into a CUDA graph (no host sync, no
+ * allocation). Return 0 on success.
+ */
+typedef int (*dg_denoise_fn)(void* user, const int32_t* canvas, const int32_t* pass,
+                             void* h_out, dg_stream_t stream);
+
+/*
+ * Built-in synthetic denoiser (test workload, not part of the method): with t = pass + 1 and
+ * a_t = min(1, fp32((2 + t)/10)), x = a_t * w[y_r] + (1 - a_t) * w[c_r] in fp32 (E4M3 rows
+ * dequantised as code * w_scale), h_r = s_r * x / ||x||_2 (0 when x = 0), s_r = s_content
+ * for the first n_content slots of each canvas and s_pad for the rest, rounded to bf16.
+ * Pass dg_synth_denoise as the hook and a dg_synth_params* (host memory, read at call time)
+ * as `user`.
+ */
+typedef struct {
+    const dg_head_desc* desc; /* head whose rows are mixed (the head is tied) */
+    const int32_t* y;         /* device [B*S] target ids */
+    int32_t n_content;
+    float s_content, s_pad;
+    uint32_t* status;         /* optional device status word (DG_ST_BAD_TOKEN on bad ids) */
+} dg_synth_params;
+
+DG_API int dg_synth_denoise(void* user, const int32_t* canvas, const int32_t* pass, void* h_out,
+                     dg_stream_t stream);
+
+/*
+ * The whole denoising loop, stream-ordered with no host synchronisation: a CUDA graph whose
+ * conditional WHILE node runs [denoise -> (quantise) -> statistics -> keep/re-randomise/stop]
+ * until every canvas has stopped or max_passes is reached.
+ *   canvas [B*S]: the canvas (in/out). If init_random, it is first overwritten with
+ *     key(seed, 0xFFFFFFFF, r) mod V.
+ *   h_buffer: device [B*S, d] buffer the denoiser writes (desc->h must equal it).
+ *   K_t = keep_sched ? keep_sched[p] : min(keep_k0 * (p + 1), S) for 0-based pass p.
+ *   state [B] (device): on entry `stable` is the resume count when start_pass > 0 (and is
+ *     reset to 0 otherwise); on exit it holds passes/reason/mean_entropy per canvas.
+ *   argmax/conf/entropy: optional device outputs of the last pass that ran.
+ *   trace_mean_entropy [max_passes * B], trace_canvas [(max_passes + 1) * B*S] (the canvas
+ *   entering pass p at row p; the final canvas after the last pass is not appended),
+ *   trace_h [max_passes * B*S*d] (bytes of h_dtype), trace_argmax/conf/entropy
+ *   [max_passes * B*S]: optional device traces of every pass, for checking.
+ */
+typedef struct {
+    dg_stop_rule rule;
+    int32_t keep_k0;
+    const int32_t* keep_sched;  /* optional device [max_passes] */
+    uint64_t seed;
+    uint32_t start_pass;
+    uint32_t init_random;
+    float* trace_mean_entropy;
+    int32_t* trace_canvas;
+    void* trace_h;
+    int32_t* trace_argmax;      /* optional device [max_passes * B*S] per-pass statistics */
+    float* trace_conf;
+    float* trace_entropy;
+} dg_loop_params;
+
+DG_API int dg_canvas_loop(const dg_head_desc* desc, int32_t* canvas, void* h_buffer,
+                   const dg_loop_params* params, dg_denoise_fn denoise, void* user,
+                   dg_canvas_state* state, int32_t* argmax, float* conf, float* entropy,
+                   void* workspace, size_t workspace_bytes, uint32_t* status,
+                   dg_stream_t stream);
+
+/*
+ * Instrumentation: make the next dg_canvas_stats / dg_canvas_step call issued by this host
+ * thread record `start_event` on its stream just before its vocabulary-head kernel and
+ * `stop_event` just after it (cudaEvent_t handles created by the caller). One-shot; calls that
+ * are being captured into a graph do not consume it. Passing NULLs clears a pending request.
+ */
+DG_API int dg_profile_next_head(void* start_event, void* stop_event);
+
+/* Human-readable name of a DG_ERR_* code or DG_ST_* bit set. */
+DG_API const char* dg_status_string(int code);
+
+/* Library version, e.g. 100 for 0.1.0. */
+DG_API int dg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DGCANVAS_H */

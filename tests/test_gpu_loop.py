@@ -1,0 +1,164 @@
+"""GPU parity of the whole denoising loop (graph with a conditional WHILE node) against the
+oracle: lockstep (the oracle recomputes every pass from the GPU's own canvas and hidden states)
+and free-run (the oracle runs the loop on its own)."""
+import numpy as np
+import pytest
+import torch
+
+from parity import GAP, TOL, check_select, check_stats, dev, dev_bf16, dev_u8, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dg():
+    from uniform_state_denoising_vocab_b300 import build
+    build.build()
+    import uniform_state_denoising_vocab_b300 as m
+    m.lib()
+    return m
+
+
+def _bf16_values(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def _gpu_kept(conf, S, K):
+    """The kept mask the GPU rule implies for its own confidences (conf desc, slot asc)."""
+    B = conf.size // S
+    kept = np.zeros(conf.size, np.uint8)
+    for b in range(B):
+        c = conf[b * S:(b + 1) * S]
+        order = np.lexsort((np.arange(S), -c.astype(np.float64)))
+        kept[b * S + order[:K]] = 1
+    return kept
+
+
+def _lockstep(dg, orc, res, cfg, w_host, w_scale_host, y, dtype, rows=None):
+    """Check every pass the GPU ran. Returns (number of passes, list of near-tie events)."""
+    R, S, V, d = cfg.R, cfg.S, cfg.V, cfg.d
+    st = dg.state_fields(res["state"])
+    P = int(st["passes"].max())
+    tc = host(res["trace_canvas"])
+    th = host(res["trace_h"].view(torch.int16)).view(np.uint16)
+    tm = host(res["trace_mean_entropy"])
+    ta, tcf, te = host(res["trace_argmax"]), host(res["trace_conf"]), host(res["trace_entropy"])
+    final = host(res["canvas"])
+    events = []
+    assert np.array_equal(tc[0], orc.draw(cfg.seed, 0xFFFFFFFF, np.arange(R), V))
+    for p in range(P):
+        c_p = tc[p]
+        c_next = tc[p + 1] if p + 1 < P else final
+        # the denoiser output matches the oracle's denoiser on the same canvas within 1 bf16 ulp
+        ho = orc.synth_denoise(cfg.B, S, d, V, dtype, w_host, y, c_p, p, cfg.n_content,
+                               cfg.s_content, cfg.s_pad, w_scale=w_scale_host)
+        hg = th[p].reshape(-1)
+        # within one bf16 ulp of the larger magnitude, plus the fp32 cancellation error of the
+        # mix a*W[y] + (1-a)*W[c] (about 1e-7 of the terms, times s/|x|): 1e-5 absolute
+        vg, vo = _bf16_values(hg).astype(np.float64), _bf16_values(ho).astype(np.float64)
+        err = np.abs(vg - vo)
+        bound = 2.0**-7 * np.maximum(np.abs(vg), np.abs(vo)) + 1e-5
+        assert (err <= bound).all(), f"pass {p}: denoiser differs by {err.max()}"
+        K = min(cfg.keep_k * (p + 1), S)
+        o = orc.step(cfg.B, S, V, d, dtype, hg, w_host, K, cfg.seed, p, w_scale=w_scale_host)
+        g = {"argmax": ta[p], "conf": tcf[p], "entropy": te[p], "canvas": c_next,
+             "kept": _gpu_kept(tcf[p], S, K)}
+        check_stats(g, o, TOL[dtype])
+        check_select(g, o, cfg.B, S, V, K, cfg.seed, p, orc.draw)
+        assert abs(tm[p][0] - o["mean_entropy"][0]) <= TOL[dtype]
+        if (g["argmax"] != o["argmax"]).any() or (g["kept"] != o["kept"]).any():
+            events.append((p, int((g["argmax"] != o["argmax"]).sum()),
+                           int((g["kept"] != o["kept"]).sum()), float(o["kgap"][0])))
+        # the stop decision at this pass agrees unless the mean entropy is within 2e-3 of theta
+        if abs(o["mean_entropy"][0] - cfg.theta) >= 2e-3:
+            stopped_here = p + 1 == P
+            ent = o["mean_entropy"][0] < cfg.theta
+            if ent:
+                assert stopped_here
+    return P, events
+
+
+def test_loop_bf16_v32768_lockstep_and_free_run(dg, orc):
+    from workloads import CONFIGS, make_loop_inputs
+    cfg = CONFIGS["loop_bf16_v32768_d256"]
+    x = make_loop_inputs(cfg)
+    tw = dev_bf16(x["w"], (cfg.V, cfg.d))
+    canvas = torch.empty(cfg.R, dtype=torch.int32, device="cuda")
+    res = dg.dg_canvas_loop(tw, canvas, B=cfg.B, S=cfg.S, theta=cfg.theta, y=dev(x["y"]),
+                            keep_k0=cfg.keep_k, seed=cfg.seed, max_passes=cfg.max_passes,
+                            stable_passes=cfg.stable_passes, n_content=cfg.n_content,
+                            s_content=cfg.s_content, s_pad=cfg.s_pad, trace=True)
+    torch.cuda.synchronize()
+    assert int(res["status"][0]) == 0
+    st = dg.state_fields(res["state"])
+    assert st["done"][0] == 1
+    P, events = _lockstep(dg, orc, res, cfg, x["w"], None, x["y"], "bf16")
+    # free run: the oracle's own loop
+    den = lambda c, p: orc.synth_denoise(cfg.B, cfg.S, cfg.d, cfg.V, "bf16", x["w"], x["y"], c, p,
+                                         cfg.n_content, cfg.s_content, cfg.s_pad)
+    ref = orc.loop(cfg.B, cfg.S, cfg.V, cfg.d, "bf16", x["w"], den, theta=cfg.theta,
+                   stable_passes=cfg.stable_passes, max_passes=cfg.max_passes,
+                   keep_k0=cfg.keep_k, seed=cfg.seed)
+    print(f"GPU passes {P} reason {int(st['reason'][0])}; oracle passes {ref['passes'][0]} "
+          f"reason {ref['reason'][0]}; near-tie events {events}")
+    if not events:
+        assert P == ref["passes"][0] and int(st["reason"][0]) == ref["reason"][0]
+        assert np.array_equal(host(res["canvas"]), ref["canvas"])
+
+
+def test_loop_graph_reuse_and_resume(dg):
+    """A second call with the same arguments reuses the captured graph and gives the same
+    result; resuming from a mid-loop canvas with its stable count reproduces the tail."""
+    from workloads import CONFIGS, make_loop_inputs
+    cfg = CONFIGS["loop_bf16_v32768_d256"]
+    x = make_loop_inputs(cfg)
+    tw = dev_bf16(x["w"], (cfg.V, cfg.d))
+    ty = dev(x["y"])
+    kw = dict(B=cfg.B, S=cfg.S, theta=cfg.theta, y=ty, keep_k0=cfg.keep_k, seed=cfg.seed,
+              max_passes=cfg.max_passes, n_content=cfg.n_content, s_content=cfg.s_content,
+              s_pad=cfg.s_pad)
+    c1 = torch.empty(cfg.R, dtype=torch.int32, device="cuda")
+    r1 = dg.dg_canvas_loop(tw, c1, trace=True, **kw)
+    torch.cuda.synchronize()
+    c1_final = c1.clone()
+    s1 = dg.state_fields(r1["state"])
+    r2 = dg.dg_canvas_loop(tw, c1, trace=True, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(c1, c1_final)
+    assert dg.state_fields(r2["state"])["passes"].tolist() == s1["passes"].tolist()
+    P = int(s1["passes"][0])
+    if P >= 3:
+        k = P - 2
+        mid = r1["trace_canvas"][k].clone()
+        # stable count entering pass k: consecutive unchanged passes before it
+        tc = host(r1["trace_canvas"])
+        stable = 0
+        for p in range(k):
+            stable = 0 if np.any(tc[p + 1] != tc[p]) else stable + 1
+        state = dg.new_state(cfg.B, "cuda")
+        state[0, 2] = stable
+        r3 = dg.dg_canvas_loop(tw, mid, init_random=False, start_pass=k, state=state, **kw)
+        torch.cuda.synchronize()
+        assert torch.equal(mid, c1_final)
+        assert dg.state_fields(r3["state"])["passes"].tolist() == s1["passes"].tolist()
+
+
+def test_loop_rules_on_device(dg):
+    """Each stop rule fires at the expected pass on the device: cap with nothing kept, entropy
+    at the first pass with large logits."""
+    V, d, S = 512, 64, 256
+    rng = np.random.default_rng(0)
+    w = torch.from_numpy((rng.standard_normal((V, d)) / 8).astype(np.float32)).to(torch.bfloat16).cuda()
+    y = torch.from_numpy(rng.integers(1, V, S).astype(np.int32)).cuda()
+    c = torch.empty(S, dtype=torch.int32, device="cuda")
+    # k0 = 0: nothing is ever kept, the canvas changes every pass -> cap at max_passes
+    r = dg.dg_canvas_loop(w, c, B=1, S=S, theta=1e-6, y=y, keep_k0=0, seed=3, max_passes=7)
+    torch.cuda.synchronize()
+    f = dg.state_fields(r["state"])
+    assert f["passes"].tolist() == [7] and f["reason"].tolist() == [dg.REASON_CAP]
+    # huge scale: every slot one-hot at pass 0 -> entropy rule at the first pass
+    r = dg.dg_canvas_loop(w, c, B=1, S=S, theta=0.05, y=y, keep_k0=0, seed=3, s_content=3000.0,
+                          s_pad=3000.0, n_content=S)
+    torch.cuda.synchronize()
+    f = dg.state_fields(r["state"])
+    assert f["passes"].tolist() == [1] and f["reason"][0] & dg.REASON_ENTROPY

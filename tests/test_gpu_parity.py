@@ -1,0 +1,252 @@
+"""GPU parity: the CUDA path (through the C ABI) against the double-precision oracle on the same
+seeded inputs, at sizes spanning several tiles with ragged tails, plus edge cases."""
+import numpy as np
+import pytest
+import torch
+
+from parity import TOL, check_select, check_stats, dev, dev_bf16, dev_u8, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dg():
+    from uniform_state_denoising_vocab_b300 import build
+    build.build()
+    import uniform_state_denoising_vocab_b300 as m
+    assert torch.cuda.is_available()
+    m.lib()
+    return m
+
+
+def _rand_case(B, S, V, d, seed, dtype, hscale=1.0):
+    rng = np.random.default_rng(seed)
+    h = (rng.standard_normal(B * S * d) * hscale).astype(np.float32)
+    w = (rng.standard_normal(V * d) / np.sqrt(d)).astype(np.float32)
+    canvas = rng.integers(0, V, B * S).astype(np.int32)
+    return h, w, canvas
+
+
+def _bits(x):
+    return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _run_step(dg, orc, B, S, V, d, dtype, K, seed, pass_, hscale=1.0, inv_temp=1.0):
+    h, w, canvas = _rand_case(B, S, V, d, seed, dtype, hscale)
+    if dtype == "f32":
+        th, tw = dev(h).view(B * S, d), dev(w).view(V, d)
+        oh, ow, ws = h, w, None
+        okw = {}
+    elif dtype == "bf16":
+        hb, wb = _bits(h), _bits(w)
+        th, tw = dev_bf16(hb, (B * S, d)), dev_bf16(wb, (V, d))
+        oh, ow = hb, wb
+        okw = {}
+    else:
+        hb = _bits(h)
+        wq, wsc = orc.quant_rows_e4m3(_bits(w), V, d)
+        th, tw = dev_bf16(hb, (B * S, d)), dev_u8(wq, (V, d))
+        oh, ow = hb, wq
+        okw = {"w_scale": wsc}
+    tws = dev(okw["w_scale"]) if "w_scale" in okw else None
+    tc = dev(canvas)
+    res = dg.dg_canvas_step(th, tw, tc, K, seed, pass_, B=B, S=S, w_scale=tws, inv_temp=inv_temp)
+    torch.cuda.synchronize()
+    g = {k: host(v) for k, v in res.items() if torch.is_tensor(v)}
+    o = orc.step(B, S, V, d, dtype, oh, ow, K, seed, pass_, w_scale=okw.get("w_scale"),
+                 inv_temp=inv_temp)
+    return g, o, canvas
+
+
+def test_fp32_pass_v4096_d64(dg, orc):
+    """Single canvas pass, fp32 head 4096 x 64, 256 slots, keep 32, seed 0, pass 0."""
+    from workloads import CONFIGS, make_pass_inputs
+    cfg = CONFIGS["pass_f32_v4096_d64"]
+    x = make_pass_inputs(cfg)
+    th = dev(x["h"]).view(cfg.R, cfg.d)
+    tw = dev(x["w"]).view(cfg.V, cfg.d)
+    res = dg.dg_canvas_step(th, tw, dev(x["canvas"]), cfg.keep_k, cfg.seed, 0, B=cfg.B, S=cfg.S)
+    torch.cuda.synchronize()
+    g = {k: host(v) for k, v in res.items() if torch.is_tensor(v)}
+    o = orc.step(cfg.B, cfg.S, cfg.V, cfg.d, "f32", x["h"], x["w"], cfg.keep_k, cfg.seed, 0)
+    check_stats(g, o, TOL["f32"])
+    check_select(g, o, cfg.B, cfg.S, cfg.V, cfg.keep_k, cfg.seed, 0, orc.draw)
+    assert int(g["status"][0]) == 0
+    assert abs(g["mean_entropy"][0] - o["mean_entropy"][0]) <= TOL["f32"]
+
+
+@pytest.mark.parametrize("B,S,V,d", [
+    (1, 256, 1000, 128),     # ragged vocabulary tail (3 full tiles + 232)
+    (3, 100, 777, 64),       # rows not a multiple of 128; canvases straddle row blocks
+    (2, 256, 4096, 256),     # several tiles, several K slices
+    (1, 37, 300, 512),       # short canvas
+    (1, 256, 256, 64),       # exactly one tile
+    (1, 256, 16, 64),        # vocabulary smaller than one 32-column chunk
+    (1, 256, 2083, 2816),    # full hidden size, ragged vocabulary
+])
+def test_bf16_shapes(dg, orc, B, S, V, d):
+    g, o, _ = _run_step(dg, orc, B, S, V, d, "bf16", K=min(32, S), seed=V + d, pass_=3)
+    check_stats(g, o, TOL["bf16"])
+    check_select(g, o, B, S, V, min(32, S), V + d, 3, orc.draw)
+    assert int(g["status"][0]) == 0
+    assert np.allclose(g["mean_entropy"], o["mean_entropy"], atol=TOL["bf16"])
+
+
+@pytest.mark.parametrize("B,S,V,d", [(1, 256, 1000, 256), (2, 130, 3001, 2816)])
+def test_fp32_shapes(dg, orc, B, S, V, d):
+    g, o, _ = _run_step(dg, orc, B, S, V, d, "f32", K=20, seed=5, pass_=1)
+    check_stats(g, o, TOL["f32"])
+    check_select(g, o, B, S, V, 20, 5, 1, orc.draw)
+
+
+@pytest.mark.parametrize("B,S,V,d", [(1, 256, 1000, 256), (2, 200, 2500, 2816)])
+def test_e4m3_quantised_head(dg, orc, B, S, V, d):
+    g, o, _ = _run_step(dg, orc, B, S, V, d, "e4m3", K=32, seed=11, pass_=0)
+    check_stats(g, o, TOL["e4m3"])
+    check_select(g, o, B, S, V, 32, 11, 0, orc.draw)
+
+
+def test_e4m3_prequantised_h_matches_device_quantiser(dg, orc):
+    """bf16 h quantised on the device must give the same statistics, bit for bit, as the
+    oracle-quantised E4M3 h passed in directly (the quantiser is exact in fp32)."""
+    B, S, V, d = 1, 256, 1500, 512
+    h, w, canvas = _rand_case(B, S, V, d, 21, "e4m3")
+    hb = _bits(h)
+    hq, hsc = orc.quant_rows_e4m3(hb, B * S, d)
+    wq, wsc = orc.quant_rows_e4m3(_bits(w), V, d)
+    tw, tws = dev_u8(wq, (V, d)), dev(wsc)
+    a = dg.dg_canvas_stats(dev_bf16(hb, (B * S, d)), tw, B=B, S=S, w_scale=tws)
+    b = dg.dg_canvas_stats(dev_u8(hq, (B * S, d)), tw, B=B, S=S, w_scale=tws, h_scale=dev(hsc))
+    torch.cuda.synchronize()
+    for k in ("argmax", "conf", "entropy", "mean_entropy"):
+        assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("K", [0, 1, 255, 256, 1000])
+def test_keep_edges(dg, orc, K):
+    g, o, canvas = _run_step(dg, orc, 2, 256, 3000, 128, "bf16", K=K, seed=7, pass_=9)
+    check_select(g, o, 2, 256, 3000, K, 7, 9, orc.draw)
+    if K == 0:
+        assert np.array_equal(g["canvas"], orc.draw(7, 9, np.arange(512), 3000))
+    if K >= 256:
+        assert np.array_equal(g["canvas"], g["argmax"])
+
+
+def test_in_place_and_stats_entry_agree(dg, orc):
+    B, S, V, d = 1, 256, 5000, 256
+    h, w, canvas = _rand_case(B, S, V, d, 3, "bf16")
+    th, tw = dev_bf16(_bits(h), (B * S, d)), dev_bf16(_bits(w), (V, d))
+    c1 = dev(canvas)
+    r1 = dg.dg_canvas_step(th, tw, c1, 32, 1, 2, B=B, S=S)
+    c2 = dev(canvas)
+    r2 = dg.dg_canvas_step(th, tw, c2, 32, 1, 2, B=B, S=S, canvas_out=c2)   # in place
+    st = dg.dg_canvas_stats(th, tw, B=B, S=S)
+    torch.cuda.synchronize()
+    assert torch.equal(r1["canvas"], c2)
+    for k in ("argmax", "conf", "entropy", "mean_entropy"):
+        assert torch.equal(r1[k], st[k]) and torch.equal(r1[k], r2[k])
+
+
+def test_deterministic(dg):
+    B, S, V, d = 2, 256, 20000, 512
+    h, w, canvas = _rand_case(B, S, V, d, 4, "bf16")
+    th, tw, tc = dev_bf16(_bits(h), (B * S, d)), dev_bf16(_bits(w), (V, d)), dev(canvas)
+    a = dg.dg_canvas_step(th, tw, tc, 40, 9, 4, B=B, S=S)
+    b = dg.dg_canvas_step(th, tw, tc, 40, 9, 4, B=B, S=S)
+    torch.cuda.synchronize()
+    for k in a:
+        if torch.is_tensor(a[k]):
+            assert torch.equal(a[k], b[k]), k
+
+
+def test_status_bits(dg):
+    B, S, V, d = 1, 256, 1000, 64
+    h, w, canvas = _rand_case(B, S, V, d, 5, "bf16")
+    th, tw = dev_bf16(_bits(h), (B * S, d)), dev_bf16(_bits(w), (V, d))
+    bad = canvas.copy()
+    bad[7] = V + 3
+    r = dg.dg_canvas_step(th, tw, dev(bad), 8, 0, 0, B=B, S=S)
+    torch.cuda.synchronize()
+    assert int(r["status"][0]) & dg.ST_BAD_TOKEN
+    h2 = h.copy()
+    h2[5 * d + 3] = np.nan
+    r = dg.dg_canvas_step(dev_bf16(_bits(h2), (B * S, d)), tw, dev(canvas), 8, 0, 0, B=B, S=S)
+    torch.cuda.synchronize()
+    assert int(r["status"][0]) & dg.ST_NONFINITE
+    assert not (int(r["status"][0]) & dg.ST_TIMEOUT)
+
+
+def test_step_state_and_stop_rule(dg, orc):
+    """dg_canvas_step with a state applies the stop test; a stopped canvas is frozen."""
+    B, S, V, d = 2, 64, 500, 64
+    rng = np.random.default_rng(8)
+    w = (rng.standard_normal(V * d) / np.sqrt(d)).astype(np.float32)
+    h = (rng.standard_normal(B * S * d) * np.repeat([200.0, 0.05], S * d)).astype(np.float32)
+    th, tw = dev_bf16(_bits(h), (B * S, d)), dev_bf16(_bits(w), (V, d))
+    state = dg.new_state(B, "cuda")
+    rule = dg.StopRule(max_passes=3, entropy_threshold=0.05, stable_passes=2, stop_mode=0)
+    c = dev(rng.integers(0, V, B * S).astype(np.int32))
+    for p in range(3):
+        prev = c.clone()
+        dg.dg_canvas_step(th, tw, c, 0, 3, p, B=B, S=S, canvas_out=c, state=state, rule=rule)
+        torch.cuda.synchronize()
+        f = dg.state_fields(state)
+        if p == 0:
+            assert f["done"].tolist() == [1, 0] and f["reason"][0] == dg.REASON_ENTROPY
+            frozen = c[:S].clone()
+        else:
+            assert torch.equal(c[:S], frozen)
+    f = dg.state_fields(state)
+    assert f["passes"].tolist() == [1, 3]
+    assert f["reason"][1] == dg.REASON_CAP
+
+
+def _sample_rows(R, n, seed):
+    return np.sort(np.random.default_rng(seed).choice(R, size=n, replace=False))
+
+
+@pytest.fixture(scope="module")
+def full_pass_inputs():
+    from workloads import CONFIGS, make_pass_inputs
+    cfg = CONFIGS["pass_bf16_v262144_d2816"]
+    return cfg, make_pass_inputs(cfg)
+
+
+def test_full_vocab_bf16_sampled_rows(dg, orc, full_pass_inputs):
+    """256 slots x 262144 vocab x d=2816 in the launch configuration the benchmark times:
+    sampled rows against the oracle one by one, every row against the invariants."""
+    cfg, x = full_pass_inputs
+    th, tw = dev_bf16(x["h"], (cfg.R, cfg.d)), dev_bf16(x["w"], (cfg.V, cfg.d))
+    res = dg.dg_canvas_step(th, tw, dev(x["canvas"]), cfg.keep_k, cfg.seed, 0, B=cfg.B, S=cfg.S)
+    torch.cuda.synchronize()
+    g = {k: host(v) for k, v in res.items() if torch.is_tensor(v)}
+    rows = _sample_rows(cfg.R, 24, 1)
+    o = orc.head_stats(cfg.R, cfg.d, cfg.V, "bf16", x["h"], x["w"], rows=rows)
+    check_stats(g, o, TOL["bf16"], rows=rows)
+    assert int(g["status"][0]) == 0
+    assert (g["entropy"] >= 0).all() and (g["entropy"] <= np.log(cfg.V) + 1e-4).all()
+    assert (g["conf"] >= 1.0 / cfg.V * 0.999).all() and (g["conf"] <= 1.0).all()
+    assert g["kept"].sum() == cfg.keep_k
+    # the kept slots are exactly the K largest GPU confidences (ties by slot)
+    order = np.lexsort((np.arange(cfg.S), -g["conf"]))
+    assert set(np.nonzero(g["kept"])[0]) == set(order[: cfg.keep_k])
+    draws = orc.draw(cfg.seed, 0, np.arange(cfg.R), cfg.V)
+    assert np.array_equal(g["canvas"], np.where(g["kept"] == 1, g["argmax"], draws))
+    assert abs(g["mean_entropy"][0] - g["entropy"].astype(np.float64).mean()) < 1e-4
+
+
+def test_batched_bf16_sampled_rows(dg, orc):
+    from workloads import CONFIGS, make_pass_inputs
+    cfg = CONFIGS["pass_bf16_b8_v262144_d2816"]
+    x = make_pass_inputs(cfg)
+    th, tw = dev_bf16(x["h"], (cfg.R, cfg.d)), dev_bf16(x["w"], (cfg.V, cfg.d))
+    res = dg.dg_canvas_step(th, tw, dev(x["canvas"]), cfg.keep_k, cfg.seed, 0, B=cfg.B, S=cfg.S)
+    torch.cuda.synchronize()
+    g = {k: host(v) for k, v in res.items() if torch.is_tensor(v)}
+    rows = _sample_rows(cfg.R, 24, 2)
+    o = orc.head_stats(cfg.R, cfg.d, cfg.V, "bf16", x["h"], x["w"], rows=rows)
+    check_stats(g, o, TOL["bf16"], rows=rows)
+    for b in range(cfg.B):
+        sl = slice(b * cfg.S, (b + 1) * cfg.S)
+        assert g["kept"][sl].sum() == cfg.keep_k
+        assert abs(g["mean_entropy"][b] - g["entropy"][sl].astype(np.float64).mean()) < 1e-4

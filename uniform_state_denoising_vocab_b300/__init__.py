@@ -1,0 +1,297 @@
+"""B300-native canvas pass of a uniform-state block text-diffusion sampler.
+
+A thin ctypes binding over libdgcanvas.so (C ABI in include/dgcanvas.h). Every step of the
+path -- the vocabulary-head contraction with its fused softmax statistics, the confidence top-K
+keep, the counter-hash re-randomisation, the stop test and the graph-driven loop -- runs in the
+library's CUDA kernels; this module only marshals torch tensors, streams and structs. There is
+no CPU fallback: if the library or a CUDA device is missing, calls raise.
+
+Names mirror the C entry points: dg_workspace_bytes, dg_canvas_stats, dg_canvas_step,
+dg_canvas_loop (plus dg_synth_denoise as the built-in denoiser hook).
+"""
+from __future__ import annotations
+
+import ctypes as C
+from pathlib import Path
+
+import torch
+
+__all__ = ["DG_F32", "DG_BF16", "DG_E4M3", "HeadDesc", "CanvasState", "StopRule", "LoopParams",
+           "SynthParams", "DgError", "lib", "dg_workspace_bytes", "dg_canvas_stats",
+           "dg_canvas_step", "dg_canvas_loop", "dg_status_string", "dtype_code", "new_state",
+           "REASON_ENTROPY", "REASON_STABLE", "REASON_CAP", "ST_BAD_TOKEN", "ST_NONFINITE",
+           "ST_TIMEOUT", "STOP_OR", "STOP_AND"]
+
+DG_F32, DG_BF16, DG_E4M3 = 0, 1, 2
+REASON_ENTROPY, REASON_STABLE, REASON_CAP = 1, 2, 4
+ST_BAD_TOKEN, ST_NONFINITE, ST_TIMEOUT = 1, 2, 4
+STOP_OR, STOP_AND = 0, 1
+
+_LIB_PATH = Path(__file__).resolve().parent / "libdgcanvas.so"
+_lib = None
+
+
+class DgError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {dg_status_string(code)} ({code})")
+
+
+class HeadDesc(C.Structure):
+    _fields_ = [("B", C.c_int32), ("S", C.c_int32), ("d", C.c_int32), ("V", C.c_int32),
+                ("h_dtype", C.c_int32), ("w_dtype", C.c_int32), ("h", C.c_void_p),
+                ("h_scale", C.c_void_p), ("w", C.c_void_p), ("w_scale", C.c_void_p),
+                ("inv_temp", C.c_float)]
+
+
+class CanvasState(C.Structure):
+    _fields_ = [("passes", C.c_int32), ("reason", C.c_int32), ("stable", C.c_int32),
+                ("done", C.c_int32), ("mean_entropy", C.c_float), ("last_pass", C.c_int32),
+                ("reserved", C.c_int32 * 2)]
+
+
+class StopRule(C.Structure):
+    _fields_ = [("max_passes", C.c_int32), ("entropy_threshold", C.c_float),
+                ("stable_passes", C.c_int32), ("stop_mode", C.c_int32)]
+
+
+class LoopParams(C.Structure):
+    _fields_ = [("rule", StopRule), ("keep_k0", C.c_int32), ("keep_sched", C.c_void_p),
+                ("seed", C.c_uint64), ("start_pass", C.c_uint32), ("init_random", C.c_uint32),
+                ("trace_mean_entropy", C.c_void_p), ("trace_canvas", C.c_void_p),
+                ("trace_h", C.c_void_p), ("trace_argmax", C.c_void_p), ("trace_conf", C.c_void_p),
+                ("trace_entropy", C.c_void_p)]
+
+
+class SynthParams(C.Structure):
+    _fields_ = [("desc", C.POINTER(HeadDesc)), ("y", C.c_void_p), ("n_content", C.c_int32),
+                ("s_content", C.c_float), ("s_pad", C.c_float), ("status", C.c_void_p)]
+
+
+DENOISE_FN = C.CFUNCTYPE(C.c_int, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p)
+
+
+def lib():
+    """Load libdgcanvas.so (built in-tree by uniform_state_denoising_vocab_b300.build)."""
+    global _lib
+    if _lib is None:
+        if not _LIB_PATH.exists():
+            raise ImportError(f"libdgcanvas.so not built at {_LIB_PATH}; run "
+                              "`python -m uniform_state_denoising_vocab_b300.build`")
+        L = C.CDLL(str(_LIB_PATH))
+        vp, sz = C.c_void_p, C.c_size_t
+        L.dg_workspace_bytes.argtypes = [C.POINTER(HeadDesc), C.POINTER(sz)]
+        L.dg_canvas_stats.argtypes = [C.POINTER(HeadDesc), vp, vp, vp, vp, vp, sz, vp, vp]
+        L.dg_canvas_step.argtypes = [C.POINTER(HeadDesc), vp, vp, C.c_int32, C.c_uint64,
+                                     C.c_uint32, vp, vp, vp, vp, vp, vp, C.POINTER(StopRule), vp,
+                                     sz, vp, vp]
+        L.dg_canvas_loop.argtypes = [C.POINTER(HeadDesc), vp, vp, C.POINTER(LoopParams), vp, vp,
+                                     vp, vp, vp, vp, vp, sz, vp, vp]
+        L.dg_status_string.argtypes = [C.c_int]
+        L.dg_status_string.restype = C.c_char_p
+        L.dg_version.restype = C.c_int
+        L.dg_profile_next_head.argtypes = [C.c_void_p, C.c_void_p]
+        L.dg_profile_next_head.restype = C.c_int
+        for f in ("dg_workspace_bytes", "dg_canvas_stats", "dg_canvas_step", "dg_canvas_loop"):
+            getattr(L, f).restype = C.c_int
+        _lib = L
+    return _lib
+
+
+def dg_profile_next_head(start: torch.cuda.Event, stop: torch.cuda.Event) -> None:
+    """Bracket the next head kernel launched by this thread with two recorded CUDA events."""
+    start.record()   # materialise the underlying cudaEvent_t handles
+    stop.record()
+    _check(lib().dg_profile_next_head(C.c_void_p(start.cuda_event), C.c_void_p(stop.cuda_event)),
+           "dg_profile_next_head")
+
+
+def dg_status_string(code: int) -> str:
+    return lib().dg_status_string(int(code)).decode()
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != 0:
+        raise DgError(rc, where)
+
+
+def dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return DG_F32
+    if t.dtype == torch.bfloat16:
+        return DG_BF16
+    if t.dtype in (torch.float8_e4m3fn, torch.uint8):
+        return DG_E4M3
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to libdgcanvas must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libdgcanvas must be contiguous")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def make_desc(h, w, *, B: int, S: int, h_scale=None, w_scale=None, inv_temp: float = 1.0,
+              h_dtype: int | None = None, d: int | None = None) -> HeadDesc:
+    """Head descriptor over torch tensors: h [B*S, d] (or None for a loop's buffer later),
+    w [V, d], optional fp32 scales for E4M3 operands."""
+    V, dd = int(w.shape[0]), int(w.shape[1])
+    hd = dtype_code(h) if h is not None else (DG_BF16 if h_dtype is None else h_dtype)
+    return HeadDesc(B=B, S=S, d=dd if d is None else d, V=V, h_dtype=hd, w_dtype=dtype_code(w),
+                    h=None if h is None else _ptr(h).value, h_scale=None if h_scale is None else
+                    _ptr(h_scale).value, w=_ptr(w).value,
+                    w_scale=None if w_scale is None else _ptr(w_scale).value,
+                    inv_temp=float(inv_temp))
+
+
+def dg_workspace_bytes(desc: HeadDesc) -> int:
+    n = C.c_size_t(0)
+    _check(lib().dg_workspace_bytes(C.byref(desc), C.byref(n)), "dg_workspace_bytes")
+    return int(n.value)
+
+
+def _workspace(desc: HeadDesc, device, workspace=None):
+    need = dg_workspace_bytes(desc)
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < need:
+            raise ValueError(f"workspace too small: need {need} bytes")
+        return workspace
+    return torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+
+
+def new_state(B: int, device) -> torch.Tensor:
+    """Device array of B dg_canvas_state records (8 int32 each), zero-initialised."""
+    return torch.zeros(B, 8, dtype=torch.int32, device=device)
+
+
+def dg_canvas_stats(h, w, *, B: int, S: int, h_scale=None, w_scale=None, inv_temp: float = 1.0,
+                    workspace=None, status=None, stream=None) -> dict:
+    """Per-slot argmax, confidence (max prob), entropy (nats) and per-canvas mean entropy."""
+    dev = w.device
+    R = B * S
+    desc = make_desc(h, w, B=B, S=S, h_scale=h_scale, w_scale=w_scale, inv_temp=inv_temp)
+    ws = _workspace(desc, dev, workspace)
+    out = {"argmax": torch.empty(R, dtype=torch.int32, device=dev),
+           "conf": torch.empty(R, dtype=torch.float32, device=dev),
+           "entropy": torch.empty(R, dtype=torch.float32, device=dev),
+           "mean_entropy": torch.empty(B, dtype=torch.float32, device=dev)}
+    st = torch.zeros(1, dtype=torch.int32, device=dev) if status is None else status
+    rc = lib().dg_canvas_stats(C.byref(desc), _ptr(out["argmax"]), _ptr(out["conf"]),
+                               _ptr(out["entropy"]), _ptr(out["mean_entropy"]), _ptr(ws),
+                               ws.numel(), _ptr(st), _stream(stream))
+    _check(rc, "dg_canvas_stats")
+    out["status"] = st
+    return out
+
+
+def dg_canvas_step(h, w, canvas_in, keep_k: int, seed: int, pass_: int, *, B: int, S: int,
+                   canvas_out=None, h_scale=None, w_scale=None, inv_temp: float = 1.0,
+                   state=None, rule: StopRule | None = None, outputs: bool = True,
+                   workspace=None, status=None, stream=None) -> dict:
+    """One canvas pass: statistics, keep the top-K by confidence, re-randomise the rest."""
+    dev = w.device
+    R = B * S
+    desc = make_desc(h, w, B=B, S=S, h_scale=h_scale, w_scale=w_scale, inv_temp=inv_temp)
+    ws = _workspace(desc, dev, workspace)
+    out = {"canvas": canvas_out if canvas_out is not None else torch.empty(R, dtype=torch.int32, device=dev)}
+    if outputs:
+        out.update({"argmax": torch.empty(R, dtype=torch.int32, device=dev),
+                    "conf": torch.empty(R, dtype=torch.float32, device=dev),
+                    "entropy": torch.empty(R, dtype=torch.float32, device=dev),
+                    "kept": torch.empty(R, dtype=torch.uint8, device=dev),
+                    "mean_entropy": torch.empty(B, dtype=torch.float32, device=dev)})
+    g = out.get
+    st = torch.zeros(1, dtype=torch.int32, device=dev) if status is None else status
+    rc = lib().dg_canvas_step(C.byref(desc), _ptr(canvas_in), _ptr(out["canvas"]), int(keep_k),
+                              C.c_uint64(seed), C.c_uint32(pass_ & 0xFFFFFFFF), _ptr(g("argmax")),
+                              _ptr(g("conf")), _ptr(g("entropy")), _ptr(g("kept")),
+                              _ptr(g("mean_entropy")), _ptr(state),
+                              None if rule is None else C.byref(rule), _ptr(ws), ws.numel(),
+                              _ptr(st), _stream(stream))
+    _check(rc, "dg_canvas_step")
+    out["status"] = st
+    return out
+
+
+def dg_canvas_loop(w, canvas, *, B: int, S: int, theta: float, y=None, denoise=None,
+                   h_buffer=None, w_scale=None, keep_k0: int = 32, keep_sched=None,
+                   seed: int = 0, max_passes: int = 48, stable_passes: int = 2,
+                   stop_mode: int = STOP_OR, start_pass: int = 0, init_random: bool = True,
+                   state=None, n_content: int = 50, s_content: float = 8.0, s_pad: float = 16.0,
+                   trace: bool = False, workspace=None, status=None, stream=None) -> dict:
+    """The whole denoising loop on the device (one graph launch, no host synchronisation).
+
+    With y given (and denoise None) the built-in synthetic denoiser is used. `denoise`, if
+    given, is a Python callable (canvas_ptr, pass_ptr, h_ptr, stream_handle) -> int that must
+    enqueue capturable work on the stream it receives.
+    """
+    dev = w.device
+    R = B * S
+    d = int(w.shape[1])
+    if h_buffer is None:
+        h_buffer = torch.empty(R, d, dtype=torch.bfloat16, device=dev)
+    desc = make_desc(h_buffer, w, B=B, S=S, w_scale=w_scale)
+    ws = _workspace(desc, dev, workspace)
+    if state is None:
+        state = new_state(B, dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev) if status is None else status
+    out = {"canvas": canvas, "state": state, "status": st, "h": h_buffer,
+           "argmax": torch.empty(R, dtype=torch.int32, device=dev),
+           "conf": torch.empty(R, dtype=torch.float32, device=dev),
+           "entropy": torch.empty(R, dtype=torch.float32, device=dev)}
+    params = LoopParams(rule=StopRule(max_passes=max_passes, entropy_threshold=theta,
+                                      stable_passes=stable_passes, stop_mode=stop_mode),
+                        keep_k0=keep_k0, keep_sched=None if keep_sched is None else _ptr(keep_sched).value,
+                        seed=seed, start_pass=start_pass, init_random=1 if init_random else 0)
+    if trace:
+        out["trace_mean_entropy"] = torch.full((max_passes, B), float("nan"), device=dev)
+        out["trace_canvas"] = torch.full((max_passes, R), -1, dtype=torch.int32, device=dev)
+        out["trace_h"] = torch.zeros(max_passes, R, d, dtype=h_buffer.dtype, device=dev)
+        params.trace_mean_entropy = _ptr(out["trace_mean_entropy"]).value
+        params.trace_canvas = _ptr(out["trace_canvas"]).value
+        params.trace_h = _ptr(out["trace_h"]).value
+        out["trace_argmax"] = torch.full((max_passes, R), -1, dtype=torch.int32, device=dev)
+        out["trace_conf"] = torch.full((max_passes, R), float("nan"), device=dev)
+        out["trace_entropy"] = torch.full((max_passes, R), float("nan"), device=dev)
+        params.trace_argmax = _ptr(out["trace_argmax"]).value
+        params.trace_conf = _ptr(out["trace_conf"]).value
+        params.trace_entropy = _ptr(out["trace_entropy"]).value
+    L = lib()
+    keep = []
+    if denoise is None:
+        if y is None:
+            raise ValueError("give y (synthetic denoiser) or a denoise callable")
+        sp = SynthParams(desc=C.pointer(desc), y=_ptr(y).value, n_content=n_content,
+                         s_content=s_content, s_pad=s_pad, status=_ptr(st).value)
+        fn = C.cast(L.dg_synth_denoise, C.c_void_p)
+        user = C.cast(C.pointer(sp), C.c_void_p)
+        keep += [sp]
+    else:
+        cb = DENOISE_FN(lambda u, c, p, h, s: int(denoise(c, p, h, s) or 0))
+        fn = C.cast(cb, C.c_void_p)
+        user = None
+        keep += [cb]
+    rc = L.dg_canvas_loop(C.byref(desc), _ptr(canvas), _ptr(h_buffer), C.byref(params), fn, user,
+                          _ptr(state), _ptr(out["argmax"]), _ptr(out["conf"]),
+                          _ptr(out["entropy"]), _ptr(ws), ws.numel(), _ptr(st), _stream(stream))
+    _check(rc, "dg_canvas_loop")
+    out["_keepalive"] = keep + [ws, desc, params]
+    return out
+
+
+def state_fields(state: torch.Tensor) -> dict:
+    """Decode a [B, 8] int32 state tensor (host copy) into named fields."""
+    s = state.detach().cpu()
+    return {"passes": s[:, 0].clone(), "reason": s[:, 1].clone(), "stable": s[:, 2].clone(),
+            "done": s[:, 3].clone(), "mean_entropy": s[:, 4].view(torch.float32).clone(),
+            "last_pass": s[:, 5].clone()}

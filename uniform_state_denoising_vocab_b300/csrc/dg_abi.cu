@@ -1,0 +1,573 @@
+// dg_abi.cu -- the extern "C" entry points declared in include/dgcanvas.h: argument
+// validation, workspace layout, launch sequencing on the caller's stream, and the graph-driven
+// denoising loop. Nothing here synchronises with the device or allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/dgcanvas.h"
+#include "dg_internal.h"
+
+namespace dg {
+
+HeadPlan plan_head(int R, int V, int d, int BM, int BN, int slots) {
+    HeadPlan p{};
+    p.R = R;
+    p.V = V;
+    p.d = d;
+    p.BM = BM;
+    p.BN = BN;
+    p.MB = (R + BM - 1) / BM;
+    p.NT = (V + BN - 1) / BN;
+    int g = slots / p.MB;
+    if (g < 1) g = 1;
+    if (g > p.NT) g = p.NT;
+    p.n_groups = g;
+    p.units = p.MB * g;
+    p.grid = p.units < slots ? p.units : slots;
+    return p;
+}
+
+namespace {
+
+enum Path { PATH_SIMT = 0, PATH_TC_BF16 = 1, PATH_TC_E4M3 = 2, PATH_TC_E4M3_QUANT = 3 };
+
+struct DeviceInfo {
+    int sms = 0;
+    bool ok = false;
+};
+
+int device_info(DeviceInfo* out) {
+    static std::mutex mu;
+    static std::vector<DeviceInfo> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DG_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(mu);
+    if (static_cast<int>(cache.size()) <= dev) cache.resize(dev + 1);
+    if (!cache[dev].ok) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return DG_ERR_CUDA;
+        if (major != 10 || minor != 3) return DG_ERR_UNSUPPORTED;
+        cache[dev].sms = sms;
+        cache[dev].ok = true;
+    }
+    *out = cache[dev];
+    return DG_OK;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int elem_size(int dt) { return dt == DG_F32 ? 4 : (dt == DG_BF16 ? 2 : 1); }
+
+// Validates the descriptor; returns the execution path or a negative error.
+int classify(const dg_head_desc* d) {
+    if (!d) return DG_ERR_INVALID_ARG;
+    if (d->B < 1 || d->S < 1 || d->d < 1 || d->V < 1) return DG_ERR_INVALID_ARG;
+    if (d->S > 1024) return DG_ERR_UNSUPPORTED;
+    if (!(d->inv_temp > 0.0f) || !(d->inv_temp < 3.0e38f)) return DG_ERR_INVALID_ARG;
+    if (static_cast<long long>(d->B) * d->S > (1ll << 30)) return DG_ERR_UNSUPPORTED;
+    if (!d->w) return DG_ERR_INVALID_ARG;
+    int path;
+    if (d->h_dtype == DG_F32 && d->w_dtype == DG_F32)
+        path = PATH_SIMT;
+    else if (d->h_dtype == DG_BF16 && d->w_dtype == DG_BF16)
+        path = PATH_TC_BF16;
+    else if (d->h_dtype == DG_E4M3 && d->w_dtype == DG_E4M3)
+        path = PATH_TC_E4M3;
+    else if (d->h_dtype == DG_BF16 && d->w_dtype == DG_E4M3)
+        path = PATH_TC_E4M3_QUANT;
+    else
+        return DG_ERR_UNSUPPORTED;
+    if (d->w_dtype == DG_E4M3 && !d->w_scale) return DG_ERR_INVALID_ARG;
+    if (d->h_dtype == DG_E4M3 && !d->h_scale) return DG_ERR_INVALID_ARG;
+    if ((static_cast<long long>(d->d) * elem_size(d->h_dtype)) % 16 != 0 ||
+        (static_cast<long long>(d->d) * elem_size(d->w_dtype)) % 16 != 0)
+        return DG_ERR_ALIGNMENT;
+    if ((d->h && !aligned16(d->h)) || !aligned16(d->w)) return DG_ERR_ALIGNMENT;
+    if ((d->h_scale && !aligned16(d->h_scale)) || (d->w_scale && !aligned16(d->w_scale)))
+        return DG_ERR_ALIGNMENT;
+    return path;
+}
+
+struct Layout {
+    HeadPlan plan;
+    size_t off_partials, off_ctl, off_qh, off_sch, total;
+};
+
+int layout_for(const dg_head_desc* d, int path, const DeviceInfo& di, Layout* L) {
+    const int R = d->B * d->S;
+    if (path == PATH_SIMT)
+        L->plan = plan_head(R, d->V, d->d, kSimtBM, kSimtBN, di.sms * 8);
+    else
+        L->plan = plan_head(R, d->V, d->d, kTcBM, kTcBN, di.sms);
+    size_t off = 0;
+    L->off_partials = off;
+    off = up256(off + static_cast<size_t>(L->plan.n_groups) * R * 16);
+    L->off_ctl = off;
+    off = up256(off + sizeof(LoopCtl));
+    L->off_qh = off;
+    L->off_sch = off;
+    if (path == PATH_TC_E4M3_QUANT) {
+        off = up256(off + static_cast<size_t>(R) * d->d);
+        L->off_sch = off;
+        off = up256(off + static_cast<size_t>(R) * 4);
+    }
+    L->total = off;
+    return DG_OK;
+}
+
+struct Prepared {
+    int path;
+    DeviceInfo di;
+    Layout L;
+};
+
+int prepare(const dg_head_desc* d, void* ws, size_t ws_bytes, Prepared* P, bool need_h = true) {
+    int path = classify(d);
+    if (path < 0) return path;
+    if (need_h && !d->h) return DG_ERR_INVALID_ARG;
+    int rc = device_info(&P->di);
+    if (rc != DG_OK) return rc;
+    P->path = path;
+    layout_for(d, path, P->di, &P->L);
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < P->L.total)
+        return DG_ERR_WORKSPACE;
+    return DG_OK;
+}
+
+thread_local cudaEvent_t t_prof_start = nullptr, t_prof_stop = nullptr;
+
+cudaError_t launch_head_only(const dg_head_desc* d, const Prepared& P, uint8_t* ws, uint32_t* status,
+                             cudaStream_t stream);
+
+// Enqueue a0 (if needed) and a1-a2 (head + partials) for the prepared descriptor, bracketing the
+// head kernel with the pending profiling events (outside graph capture only).
+cudaError_t enqueue_head(const dg_head_desc* d, const Prepared& P, uint8_t* ws, uint32_t* status,
+                         cudaStream_t stream) {
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (t_prof_start && t_prof_stop) {
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone) {
+            e0 = t_prof_start;
+            e1 = t_prof_stop;
+            t_prof_start = t_prof_stop = nullptr;
+        }
+    }
+    if (!e0) return launch_head_only(d, P, ws, status, stream);
+    // a0 runs before the bracket so that the events time the head kernel alone
+    if (P.path == PATH_TC_E4M3_QUANT) {
+        const HeadPlan& pl = P.L.plan;
+        cudaError_t e = launch_quant_rows(static_cast<const uint16_t*>(d->h), pl.R, pl.d,
+                                          ws + P.L.off_qh, reinterpret_cast<float*>(ws + P.L.off_sch),
+                                          status, stream);
+        if (e != cudaSuccess) return e;
+    }
+    cudaEventRecord(e0, stream);
+    Prepared Q = P;
+    if (Q.path == PATH_TC_E4M3_QUANT) Q.path = -PATH_TC_E4M3_QUANT;  // quantisation already done
+    cudaError_t e = launch_head_only(d, Q, ws, status, stream);
+    cudaEventRecord(e1, stream);
+    return e;
+}
+
+cudaError_t launch_head_only(const dg_head_desc* d, const Prepared& P, uint8_t* ws, uint32_t* status,
+                             cudaStream_t stream) {
+    const HeadPlan& pl = P.L.plan;
+    HeadArgs a{};
+    a.R = pl.R;
+    a.V = pl.V;
+    a.d = pl.d;
+    a.MB = pl.MB;
+    a.NT = pl.NT;
+    a.n_groups = pl.n_groups;
+    a.crow_base = d->inv_temp * 1.4426950408889634f;
+    a.partials = reinterpret_cast<float4*>(ws + P.L.off_partials);
+    a.status = status;
+    a.w_scale = d->w_scale;
+    a.h_scale = d->h_scale;
+    cudaError_t e = cudaSuccess;
+    switch (P.path) {
+    case PATH_SIMT:
+        a.num_kb = 0;
+        return launch_head_simt(static_cast<const float*>(d->h), static_cast<const float*>(d->w), a,
+                                pl.grid, stream);
+    case PATH_TC_BF16:
+        a.num_kb = (pl.d + 63) / 64;
+        return launch_head_tc(0, d->h, d->w, a, pl.grid, stream);
+    case PATH_TC_E4M3:
+        a.num_kb = (pl.d + 127) / 128;
+        return launch_head_tc(1, d->h, d->w, a, pl.grid, stream);
+    case PATH_TC_E4M3_QUANT:
+    case -PATH_TC_E4M3_QUANT: {
+        uint8_t* qh = ws + P.L.off_qh;
+        float* sch = reinterpret_cast<float*>(ws + P.L.off_sch);
+        if (P.path > 0) {
+            e = launch_quant_rows(static_cast<const uint16_t*>(d->h), pl.R, pl.d, qh, sch, status,
+                                  stream);
+            if (e != cudaSuccess) return e;
+        }
+        a.h_scale = sch;
+        a.num_kb = (pl.d + 127) / 128;
+        return launch_head_tc(1, qh, d->w, a, pl.grid, stream);
+    }
+    }
+    return cudaErrorInvalidValue;
+}
+
+SelectArgs base_select(const dg_head_desc* d, const Prepared& P, uint8_t* ws, uint32_t* status) {
+    SelectArgs s{};
+    s.partials = reinterpret_cast<const float4*>(ws + P.L.off_partials);
+    s.n_groups = P.L.plan.n_groups;
+    s.R = d->B * d->S;
+    s.S = d->S;
+    s.B = d->B;
+    s.V = d->V;
+    s.keep_k0 = -1;
+    s.status = status;
+    return s;
+}
+
+}  // namespace
+}  // namespace dg
+
+using namespace dg;
+
+extern "C" {
+
+int dg_version(void) { return 100; }
+
+int dg_profile_next_head(void* start_event, void* stop_event) {
+    if ((start_event == nullptr) != (stop_event == nullptr)) return DG_ERR_INVALID_ARG;
+    t_prof_start = static_cast<cudaEvent_t>(start_event);
+    t_prof_stop = static_cast<cudaEvent_t>(stop_event);
+    return DG_OK;
+}
+
+const char* dg_status_string(int code) {
+    switch (code) {
+    case DG_OK: return "DG_OK";
+    case DG_ERR_INVALID_ARG: return "DG_ERR_INVALID_ARG: null, negative or inconsistent argument";
+    case DG_ERR_ALIGNMENT: return "DG_ERR_ALIGNMENT: pointer not 16-byte aligned or d*elem_size % 16 != 0";
+    case DG_ERR_UNSUPPORTED: return "DG_ERR_UNSUPPORTED: device is not sm_103, dtype pair or size unsupported";
+    case DG_ERR_WORKSPACE: return "DG_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case DG_ERR_CUDA: return "DG_ERR_CUDA: a CUDA call or kernel launch failed";
+    case DG_ST_BAD_TOKEN: return "DG_ST_BAD_TOKEN: token id outside [0, V)";
+    case DG_ST_NONFINITE: return "DG_ST_NONFINITE: non-finite logit or hidden value";
+    case DG_ST_TIMEOUT: return "DG_ST_TIMEOUT: a bounded on-device wait ran out";
+    default: return "unknown status";
+    }
+}
+
+int dg_workspace_bytes(const dg_head_desc* desc, size_t* bytes) {
+    if (!bytes) return DG_ERR_INVALID_ARG;
+    int path = classify(desc);
+    if (path < 0) return path;
+    DeviceInfo di;
+    int rc = device_info(&di);
+    if (rc != DG_OK) return rc;
+    Layout L;
+    layout_for(desc, path, di, &L);
+    *bytes = L.total;
+    return DG_OK;
+}
+
+int dg_canvas_stats(const dg_head_desc* desc, int32_t* argmax, float* conf, float* entropy,
+                    float* mean_entropy, void* workspace, size_t workspace_bytes, uint32_t* status,
+                    dg_stream_t stream) {
+    Prepared P;
+    int rc = prepare(desc, workspace, workspace_bytes, &P);
+    if (rc != DG_OK) return rc;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (enqueue_head(desc, P, ws, status, st) != cudaSuccess) return DG_ERR_CUDA;
+    SelectArgs s = base_select(desc, P, ws, status);
+    s.argmax = argmax;
+    s.conf = conf;
+    s.entropy = entropy;
+    s.mean_entropy = mean_entropy;
+    if (launch_select(s, st) != cudaSuccess) return DG_ERR_CUDA;
+    return DG_OK;
+}
+
+int dg_canvas_step(const dg_head_desc* desc, const int32_t* canvas_in, int32_t* canvas_out,
+                   int32_t keep_k, uint64_t seed, uint32_t pass, int32_t* argmax, float* conf,
+                   float* entropy, uint8_t* kept, float* mean_entropy, dg_canvas_state* state,
+                   const dg_stop_rule* rule, void* workspace, size_t workspace_bytes,
+                   uint32_t* status, dg_stream_t stream) {
+    if (!canvas_in || !canvas_out || keep_k < 0) return DG_ERR_INVALID_ARG;
+    if (state && !rule) return DG_ERR_INVALID_ARG;
+    if (rule && (rule->max_passes < 1 || rule->stable_passes < 1 ||
+                 (rule->stop_mode != DG_STOP_OR && rule->stop_mode != DG_STOP_AND)))
+        return DG_ERR_INVALID_ARG;
+    Prepared P;
+    int rc = prepare(desc, workspace, workspace_bytes, &P);
+    if (rc != DG_OK) return rc;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (enqueue_head(desc, P, ws, status, st) != cudaSuccess) return DG_ERR_CUDA;
+    SelectArgs s = base_select(desc, P, ws, status);
+    s.argmax = argmax;
+    s.conf = conf;
+    s.entropy = entropy;
+    s.mean_entropy = mean_entropy;
+    s.kept = kept;
+    s.canvas_in = canvas_in;
+    s.canvas_out = canvas_out;
+    s.keep_k = keep_k;
+    s.seed = seed;
+    s.pass = pass;
+    s.state = state;
+    if (rule) {
+        s.rule = *rule;
+        s.has_rule = 1;
+    }
+    if (launch_select(s, st) != cudaSuccess) return DG_ERR_CUDA;
+    return DG_OK;
+}
+
+int dg_synth_denoise(void* user, const int32_t* canvas, const int32_t* pass, void* h_out,
+                     dg_stream_t stream) {
+    const dg_synth_params* sp = static_cast<const dg_synth_params*>(user);
+    if (!sp || !sp->desc || !sp->y || !canvas || !pass || !h_out) return DG_ERR_INVALID_ARG;
+    const dg_head_desc* d = sp->desc;
+    if (d->w_dtype == DG_F32 || d->h_dtype == DG_F32 || d->h_dtype == DG_E4M3)
+        return DG_ERR_UNSUPPORTED;  // writes bf16 hidden states from a bf16 or e4m3 head
+    if (launch_synth_denoise(d, sp->y, sp->n_content, sp->s_content, sp->s_pad, canvas, pass,
+                             static_cast<uint16_t*>(h_out), sp->status,
+                             reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return DG_ERR_CUDA;
+    return DG_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------------------------
+// The loop: a graph with one conditional WHILE node whose body is
+//   denoise -> [trace h] -> [quantise h] -> head -> select (advances the pass, sets condition).
+// ---------------------------------------------------------------------------------------------
+namespace dg {
+namespace {
+
+struct LoopKey {
+    dg_head_desc desc;
+    int32_t* canvas;
+    void* h_buffer;
+    dg_loop_params params;
+    dg_denoise_fn fn;
+    void* user;
+    dg_synth_params synth;  // content of `user` when fn is the built-in denoiser
+    dg_canvas_state* state;
+    int32_t* argmax;
+    float* conf;
+    float* entropy;
+    void* ws;
+    uint32_t* status;
+    int device;
+};
+
+struct LoopEntry {
+    LoopKey key;
+    dg_head_desc synth_desc;  // copy the built-in denoiser's desc pointer refers to
+    dg_synth_params synth_user;
+    cudaGraphExec_t exec = nullptr;
+    cudaEvent_t done = nullptr;
+    unsigned long long stamp = 0;
+};
+
+std::mutex g_loop_mu;
+std::vector<LoopEntry*> g_loops;
+unsigned long long g_stamp = 0;
+constexpr size_t kLoopCache = 16;
+
+bool same_key(const LoopKey& a, const LoopKey& b) { return std::memcmp(&a, &b, sizeof(LoopKey)) == 0; }
+
+cudaStream_t capture_stream() {
+    static std::mutex mu;
+    static std::vector<cudaStream_t> streams;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(mu);
+    if (static_cast<int>(streams.size()) <= dev) streams.resize(dev + 1, nullptr);
+    if (!streams[dev]) cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking);
+    return streams[dev];
+}
+
+int build_loop_graph(LoopEntry* E, const Prepared& P) {
+    const LoopKey& k = E->key;
+    const dg_head_desc* d = &k.desc;
+    uint8_t* ws = static_cast<uint8_t*>(k.ws);
+    LoopCtl* ctl = reinterpret_cast<LoopCtl*>(ws + P.L.off_ctl);
+
+    cudaGraph_t g = nullptr;
+    if (cudaGraphCreate(&g, 0) != cudaSuccess) return DG_ERR_CUDA;
+    cudaGraphConditionalHandle handle;
+    if (cudaGraphConditionalHandleCreate(&handle, g, 1, cudaGraphCondAssignDefault) != cudaSuccess) {
+        cudaGraphDestroy(g);
+        return DG_ERR_CUDA;
+    }
+    alignas(cudaGraphNodeParams) unsigned char np_storage[sizeof(cudaGraphNodeParams)] = {};
+    cudaGraphNodeParams& np = *reinterpret_cast<cudaGraphNodeParams*>(np_storage);
+    np.type = cudaGraphNodeTypeConditional;
+    np.conditional.handle = handle;
+    np.conditional.type = cudaGraphCondTypeWhile;
+    np.conditional.size = 1;
+    cudaGraphNode_t node;
+    if (cudaGraphAddNode(&node, g, nullptr, nullptr, 0, &np) != cudaSuccess) {
+        cudaGraphDestroy(g);
+        return DG_ERR_CUDA;
+    }
+    cudaGraph_t body = np.conditional.phGraph_out[0];
+    cudaStream_t cs = capture_stream();
+    if (!cs || cudaStreamBeginCaptureToGraph(cs, body, nullptr, nullptr, 0,
+                                             cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        cudaGraphDestroy(g);
+        return DG_ERR_CUDA;
+    }
+    int rc = DG_OK;
+    void* user = (k.fn == dg_synth_denoise) ? static_cast<void*>(&E->synth_user) : k.user;
+    if (k.fn(user, k.canvas, &ctl->pass, k.h_buffer, reinterpret_cast<dg_stream_t>(cs)) != 0)
+        rc = DG_ERR_CUDA;
+    const size_t hbytes = static_cast<size_t>(d->B) * d->S * d->d * elem_size(d->h_dtype);
+    if (rc == DG_OK && k.params.trace_h &&
+        launch_trace_copy(k.h_buffer, k.params.trace_h, hbytes, ctl, cs) != cudaSuccess)
+        rc = DG_ERR_CUDA;
+    if (rc == DG_OK && enqueue_head(d, P, ws, k.status, cs) != cudaSuccess) rc = DG_ERR_CUDA;
+    if (rc == DG_OK) {
+        SelectArgs s = base_select(d, P, ws, k.status);
+        s.argmax = k.argmax;
+        s.conf = k.conf;
+        s.entropy = k.entropy;
+        s.canvas_in = k.canvas;
+        s.canvas_out = k.canvas;
+        s.keep_k0 = k.params.keep_k0;
+        s.keep_sched = k.params.keep_sched;
+        s.seed = k.params.seed;
+        s.state = k.state;
+        s.rule = k.params.rule;
+        s.has_rule = 1;
+        s.ctl = ctl;
+        s.cond = handle;
+        s.set_cond = 1;
+        s.trace_mean_entropy = k.params.trace_mean_entropy;
+        s.trace_canvas = k.params.trace_canvas;
+        s.trace_argmax = k.params.trace_argmax;
+        s.trace_conf = k.params.trace_conf;
+        s.trace_entropy = k.params.trace_entropy;
+        if (launch_select(s, cs) != cudaSuccess) rc = DG_ERR_CUDA;
+    }
+    cudaGraph_t captured = nullptr;
+    if (cudaStreamEndCapture(cs, &captured) != cudaSuccess) rc = DG_ERR_CUDA;
+    if (rc == DG_OK && cudaGraphInstantiate(&E->exec, g, 0) != cudaSuccess) rc = DG_ERR_CUDA;
+    cudaGraphDestroy(g);
+    if (rc == DG_OK && cudaEventCreateWithFlags(&E->done, cudaEventDisableTiming) != cudaSuccess)
+        rc = DG_ERR_CUDA;
+    return rc;
+}
+
+void evict_finished_locked() {
+    // Drop the oldest entries whose last launch has completed (never blocks).
+    while (g_loops.size() > kLoopCache) {
+        size_t oldest = g_loops.size();
+        for (size_t i = 0; i < g_loops.size(); ++i)
+            if (cudaEventQuery(g_loops[i]->done) == cudaSuccess &&
+                (oldest == g_loops.size() || g_loops[i]->stamp < g_loops[oldest]->stamp))
+                oldest = i;
+        if (oldest == g_loops.size()) return;
+        LoopEntry* e = g_loops[oldest];
+        cudaGraphExecDestroy(e->exec);
+        cudaEventDestroy(e->done);
+        delete e;
+        g_loops.erase(g_loops.begin() + oldest);
+    }
+}
+
+}  // namespace
+}  // namespace dg
+
+extern "C" int dg_canvas_loop(const dg_head_desc* desc, int32_t* canvas, void* h_buffer,
+                              const dg_loop_params* params, dg_denoise_fn denoise, void* user,
+                              dg_canvas_state* state, int32_t* argmax, float* conf, float* entropy,
+                              void* workspace, size_t workspace_bytes, uint32_t* status,
+                              dg_stream_t stream) {
+    using namespace dg;
+    if (!desc || !canvas || !h_buffer || !params || !denoise || !state) return DG_ERR_INVALID_ARG;
+    if (desc->h != h_buffer) return DG_ERR_INVALID_ARG;
+    const dg_stop_rule& r = params->rule;
+    if (r.max_passes < 1 || r.stable_passes < 1 ||
+        (r.stop_mode != DG_STOP_OR && r.stop_mode != DG_STOP_AND))
+        return DG_ERR_INVALID_ARG;
+    if (params->keep_k0 < 0 || static_cast<int64_t>(params->start_pass) >= r.max_passes)
+        return DG_ERR_INVALID_ARG;
+    if (!aligned16(h_buffer) || !aligned16(canvas)) return DG_ERR_ALIGNMENT;
+    Prepared P;
+    int rc = prepare(desc, workspace, workspace_bytes, &P);
+    if (rc != DG_OK) return rc;
+    if (denoise == dg_synth_denoise && (!user || static_cast<dg_synth_params*>(user)->desc == nullptr))
+        return DG_ERR_INVALID_ARG;
+
+    LoopKey key;
+    std::memset(&key, 0, sizeof(key));
+    key.desc = *desc;
+    key.canvas = canvas;
+    key.h_buffer = h_buffer;
+    key.params = *params;
+    key.fn = denoise;
+    key.user = user;
+    if (denoise == dg_synth_denoise) key.synth = *static_cast<dg_synth_params*>(user);
+    key.state = state;
+    key.argmax = argmax;
+    key.conf = conf;
+    key.entropy = entropy;
+    key.ws = workspace;
+    key.status = status;
+    cudaGetDevice(&key.device);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    LoopCtl* ctl = reinterpret_cast<LoopCtl*>(static_cast<uint8_t*>(workspace) + P.L.off_ctl);
+
+    std::lock_guard<std::mutex> lk(g_loop_mu);
+    LoopEntry* E = nullptr;
+    // A user-supplied denoiser may read state behind `user` when it is captured, so only the
+    // built-in denoiser (whose parameters are part of the key) reuses a captured graph.
+    if (denoise == dg_synth_denoise)
+        for (LoopEntry* e : g_loops)
+            if (same_key(e->key, key)) E = e;
+    if (!E) {
+        E = new LoopEntry();
+        E->key = key;
+        if (denoise == dg_synth_denoise) {
+            E->synth_desc = *key.synth.desc;
+            E->synth_user = key.synth;
+            E->synth_user.desc = &E->synth_desc;
+        }
+        rc = build_loop_graph(E, P);
+        if (rc != DG_OK) {
+            if (E->exec) cudaGraphExecDestroy(E->exec);
+            if (E->done) cudaEventDestroy(E->done);
+            delete E;
+            return rc;
+        }
+        g_loops.push_back(E);
+    }
+    E->stamp = ++g_stamp;
+    const int R = desc->B * desc->S;
+    if (launch_loop_init(canvas, R, desc->S, desc->B, desc->V, params->seed, params->init_random ? 1 : 0,
+                         state, params->start_pass > 0 ? 1 : 0, ctl,
+                         static_cast<int>(params->start_pass), r.max_passes, status, st) != cudaSuccess)
+        return DG_ERR_CUDA;
+    if (cudaGraphLaunch(E->exec, st) != cudaSuccess) return DG_ERR_CUDA;
+    if (cudaEventRecord(E->done, st) != cudaSuccess) return DG_ERR_CUDA;
+    if (denoise != dg_synth_denoise) {
+        // not reusable: keep it until its launch has finished, then let eviction drop it
+        E->stamp = 0;
+    }
+    evict_finished_locked();
+    return DG_OK;
+}

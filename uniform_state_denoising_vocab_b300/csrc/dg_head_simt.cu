@@ -1,0 +1,89 @@
+// dg_head_simt.cu -- fp32 vocabulary head on the CUDA cores, with the same online-softmax
+// epilogue as the tensor-core head. Used for fp32 operands, which the tensor cores would round
+// (tf32); it serves small heads (hidden size 64, vocabulary 4096 in the fp32 workload).
+//
+// One CTA of 128 threads per (row block, vocabulary group) unit: thread t owns slot row
+// mb*128 + t, keeps 32 hidden values of its row in registers, and accumulates 64 logits per
+// vocabulary tile against a 64 x 32 slice of W staged in shared memory (broadcast reads).
+#include <cuda_runtime.h>
+
+#include "dg_common.cuh"
+#include "dg_internal.h"
+
+namespace dg {
+namespace {
+
+constexpr int BM = kSimtBM;  // 128 rows per CTA
+constexpr int BN = kSimtBN;  // 64 vocabulary columns per tile
+constexpr int KC = 32;       // hidden values per staging step
+
+__global__ void __launch_bounds__(BM)
+    head_simt_kernel(const float* __restrict__ h, const float* __restrict__ w, const HeadArgs args) {
+    __shared__ __align__(16) float ws[BN][KC];
+    const int t = threadIdx.x;
+    const int units = args.MB * args.n_groups;
+    for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
+        const int mb = unit % args.MB, grp = unit / args.MB;
+        const int row = mb * BM + t;
+        const bool row_ok = row < args.R;
+        const float crow = args.crow_base;
+        RowState st = row_state_init();
+        for (int nb = grp; nb < args.NT; nb += args.n_groups) {
+            float acc[BN];
+#pragma unroll
+            for (int j = 0; j < BN; ++j) acc[j] = 0.f;
+            for (int k0 = 0; k0 < args.d; k0 += KC) {
+                float hr[KC];
+#pragma unroll
+                for (int j = 0; j < KC; ++j) {
+                    const int k = k0 + j;
+                    hr[j] = (row_ok && k < args.d) ? h[static_cast<size_t>(row) * args.d + k] : 0.f;
+                }
+                __syncthreads();
+                for (int i = t; i < BN * KC; i += BM) {
+                    const int n = nb * BN + i / KC, k = k0 + i % KC;
+                    ws[i / KC][i % KC] =
+                        (n < args.V && k < args.d) ? w[static_cast<size_t>(n) * args.d + k] : 0.f;
+                }
+                __syncthreads();
+#pragma unroll
+                for (int n = 0; n < BN; ++n) {
+                    const float4* wr = reinterpret_cast<const float4*>(ws[n]);
+                    float a = acc[n];
+#pragma unroll
+                    for (int q = 0; q < KC / 4; ++q) {
+                        const float4 v = wr[q];
+                        a = fmaf(hr[4 * q + 0], v.x, a);
+                        a = fmaf(hr[4 * q + 1], v.y, a);
+                        a = fmaf(hr[4 * q + 2], v.z, a);
+                        a = fmaf(hr[4 * q + 3], v.w, a);
+                    }
+                    acc[n] = a;
+                }
+            }
+            const int valid_tile = args.V - nb * BN;
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = acc[c * 32 + j];
+                const int valid = valid_tile - c * 32;
+                if (valid >= 32)
+                    row_state_update<false>(st, v, crow, nb * BN + c * 32, 32);
+                else if (valid > 0)
+                    row_state_update<true>(st, v, crow, nb * BN + c * 32, valid);
+            }
+        }
+        if (row_ok) args.partials[static_cast<size_t>(grp) * args.R + row] = pack(row_state_partial(st));
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_head_simt(const float* h, const float* w, const HeadArgs& args, int grid,
+                             cudaStream_t stream) {
+    head_simt_kernel<<<grid, BM, 0, stream>>>(h, w, args);
+    return cudaGetLastError();
+}
+
+}  // namespace dg

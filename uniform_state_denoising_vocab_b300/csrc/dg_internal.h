@@ -1,0 +1,110 @@
+// dg_internal.h -- host-side launch interfaces between the C ABI (dg_abi.cu) and the kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/dgcanvas.h"
+
+namespace dg {
+
+// Tile geometry of the tensor-core head: 128 slot rows x 256 vocabulary columns per tile, one
+// 128-byte K slice (64 bf16 or 128 e4m3 elements) per pipeline stage.
+constexpr int kTcBM = 128;
+constexpr int kTcBN = 256;
+constexpr int kTcStages = 4;
+constexpr int kTcThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+// Geometry of the fp32 CUDA-core head.
+constexpr int kSimtBM = 128;
+constexpr int kSimtBN = 64;
+
+// Work decomposition of a head pass: MB row blocks x NT vocabulary tiles, each row block split
+// into n_groups vocabulary groups (group g takes tiles g, g + n_groups, ...). A (row block,
+// group) unit writes one Partial per row into partials[g * R + row].
+struct HeadPlan {
+    int R, V, d;
+    int BM, BN;
+    int MB, NT, n_groups, units, grid;
+};
+
+HeadPlan plan_head(int R, int V, int d, int BM, int BN, int num_sms);
+
+struct HeadArgs {
+    int R, V, d;
+    int MB, NT, n_groups, num_kb;
+    float crow_base;          // inv_temp * log2(e)
+    const float* h_scale;     // [R] or null
+    const float* w_scale;     // [V] or null
+    float4* partials;         // [n_groups][R]
+    uint32_t* status;         // sticky status word or null
+};
+
+// Tensor-core head (bf16: kind = 0, e4m3: kind = 1). h and w are device row-major matrices.
+cudaError_t launch_head_tc(int kind, const void* h, const void* w, const HeadArgs& args,
+                           int grid, cudaStream_t stream);
+// fp32 CUDA-core head.
+cudaError_t launch_head_simt(const float* h, const float* w, const HeadArgs& args, int grid,
+                             cudaStream_t stream);
+
+// Loop control block in the workspace (device).
+struct LoopCtl {
+    int32_t pass;       // index of the pass about to run
+    uint32_t ticket;    // CTAs of the select kernel finished in this pass
+    int32_t max_passes;
+    int32_t pad;
+};
+
+struct SelectArgs {
+    const float4* partials;
+    int n_groups, R, S, B, V;
+    float inv_crow_base;              // 1 / (inv_temp * log2 e): unused, kept for clarity
+    int32_t* argmax;                  // outputs, each may be null
+    float* conf;
+    float* entropy;
+    float* mean_entropy;
+    uint8_t* kept;
+    const int32_t* canvas_in;         // null: statistics only
+    int32_t* canvas_out;
+    int keep_k;                       // fixed K when keep_k0 < 0
+    int keep_k0;                      // >= 0: K_t = min(keep_k0 * (p + 1), S)
+    const int32_t* keep_sched;        // optional [max_passes]
+    uint64_t seed;
+    uint32_t pass;                    // host pass index when ctl == null
+    dg_canvas_state* state;           // optional [B]
+    dg_stop_rule rule;
+    int has_rule;
+    LoopCtl* ctl;                     // loop mode: pass from ctl, advance it, set condition
+    cudaGraphConditionalHandle cond;
+    int set_cond;
+    float* trace_mean_entropy;        // optional [max_passes * B]
+    int32_t* trace_canvas;            // optional [max_passes * R]
+    int32_t* trace_argmax;            // optional [max_passes * R] (loop mode)
+    float* trace_conf;
+    float* trace_entropy;
+    uint32_t* status;
+};
+
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream);
+
+// Per-row absmax E4M3 quantisation of bf16 rows.
+cudaError_t launch_quant_rows(const uint16_t* h, int R, int d, uint8_t* q, float* scale,
+                              uint32_t* status, cudaStream_t stream);
+
+// Loop set-up: optional random initial canvas, state reset, control block reset.
+cudaError_t launch_loop_init(int32_t* canvas, int R, int S, int B, int V, uint64_t seed,
+                             int init_random, dg_canvas_state* state, int keep_stable,
+                             LoopCtl* ctl, int start_pass, int max_passes, uint32_t* status,
+                             cudaStream_t stream);
+
+// Copy rows of one pass into a trace buffer at offset pass * bytes (pass read on device).
+cudaError_t launch_trace_copy(const void* src, void* dst, size_t bytes, const LoopCtl* ctl,
+                              cudaStream_t stream);
+
+// Built-in synthetic denoiser.
+cudaError_t launch_synth_denoise(const dg_head_desc* desc, const int32_t* y, int n_content,
+                                 float s_content, float s_pad, const int32_t* canvas,
+                                 const int32_t* pass, uint16_t* h_out, uint32_t* status,
+                                 cudaStream_t stream);
+
+}  // namespace dg
