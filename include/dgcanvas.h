@@ -214,6 +214,28 @@ DG_API int dg_canvas_loop(const dg_head_desc* desc, int32_t* canvas, void* h_buf
                    dg_stream_t stream);
 
 /*
+ * dg_canvas_step without a caller-supplied workspace, for callers that cannot allocate device
+ * memory: code running under CUDA graph stream capture (where cudaMalloc is not allowed), plugins
+ * hosted by a framework that owns all device allocations, and latency-critical code that must not
+ * risk the implicit synchronisation of cudaMalloc/cudaFree. (The pages describe no such entry
+ * point; it has no counterpart in the method.)
+ * Same arguments and results as dg_canvas_step minus the workspace. Its scratch is one array of
+ * DG_NOALLOC_SCRATCH_BYTES compiled into the library (held by every GPU that loads it until the
+ * process exits); descriptors needing more scratch than that (dg_workspace_bytes) are rejected
+ * with DG_ERR_WORKSPACE. The function allocates nothing. Its first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress), so make that first call before any stream
+ * capture. All calls share the array: calls that overlap on the GPU (unordered streams or
+ * threads) race and corrupt each other's results, so order them on one stream. Nothing in the
+ * array needs clearing between calls: each pass rewrites every scratch byte it reads.
+ */
+#define DG_NOALLOC_SCRATCH_BYTES (4u << 20)
+DG_API int dg_canvas_step_noalloc(const dg_head_desc* desc, const int32_t* canvas_in,
+                                  int32_t* canvas_out, int32_t keep_k, uint64_t seed,
+                                  uint32_t pass, int32_t* argmax, float* conf, float* entropy,
+                                  uint8_t* kept, float* mean_entropy, dg_canvas_state* state,
+                                  const dg_stop_rule* rule, uint32_t* status, dg_stream_t stream);
+
+/*
  * Instrumentation: make the next dg_canvas_stats / dg_canvas_step call issued by this host
  * thread record `start_event` on its stream just before its vocabulary-head kernel and
  * `stop_event` just after it (cudaEvent_t handles created by the caller). One-shot; calls that
