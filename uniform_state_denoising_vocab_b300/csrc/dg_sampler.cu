@@ -24,46 +24,63 @@
 namespace dg {
 namespace {
 
-__device__ __forceinline__ float block_reduce_sum_pow2(float* sh, float v) {
-    // Fixed-order pairwise tree over blockDim.x (a power of two) values.
-    const int j = threadIdx.x;
-    sh[j] = v;
-    __syncthreads();
-    for (int off = blockDim.x >> 1; off > 0; off >>= 1) {
-        if (j < off) sh[j] += sh[j + off];
-        __syncthreads();
-    }
-    const float r = sh[0];
-    __syncthreads();
-    return r;
+__device__ __forceinline__ Partial shfl_xor_partial(const Partial& p, int off) {
+    Partial q;
+    q.mx = __shfl_xor_sync(0xffffffffu, p.mx, off);
+    q.s = __shfl_xor_sync(0xffffffffu, p.s, off);
+    q.u = __shfl_xor_sync(0xffffffffu, p.u, off);
+    q.idx = __shfl_xor_sync(0xffffffffu, p.idx, off);
+    return q;
 }
 
-__global__ void select_kernel(const SelectArgs a) {
-    extern __shared__ float sh[];  // [2 * blockDim.x]: reduction scratch, confidences
+// One CTA per canvas, `tpr` (1..8, a power of two) consecutive threads per slot row:
+// the threads of a row merge disjoint, strided subsets of the vocabulary-group partials with
+// their loads batched, then combine them with a fixed xor butterfly (lower sub-lane first), so
+// every run merges in the same order.
+__global__ void __launch_bounds__(1024) select_kernel(const SelectArgs a, int tpr) {
+    extern __shared__ float sh[];  // [2 * rows_pow2]: reduction scratch, confidences
+    const int rows_pow2 = blockDim.x / tpr;
     float* sh_red = sh;
-    float* sh_conf = sh + blockDim.x;
-    const int b = blockIdx.x, j = threadIdx.x;
+    float* sh_conf = sh + rows_pow2;
+    const int b = blockIdx.x;
+    const int j = threadIdx.x / tpr;       // slot
+    const int sub = threadIdx.x % tpr;
     const bool act = j < a.S;
     const int r = b * a.S + j;
     const int p = a.ctl ? a.ctl->pass : static_cast<int>(a.pass);
 
     const bool frozen = a.state != nullptr && a.state[b].done != 0;
     if (frozen) {
-        if (act && a.canvas_out && a.canvas_out != a.canvas_in) a.canvas_out[r] = a.canvas_in[r];
+        if (act && sub == 0 && a.canvas_out && a.canvas_out != a.canvas_in)
+            a.canvas_out[r] = a.canvas_in[r];
     } else {
-        // ---- merge the partials of this row (fixed group order) ----
+        // ---- merge the partials of this row ----
         Partial acc = partial_empty();
         if (act) {
-            for (int g = 0; g < a.n_groups; ++g)
-                acc = partial_merge(acc, unpack(__ldg(a.partials + static_cast<size_t>(g) * a.R + r)));
+            const size_t stride = static_cast<size_t>(a.R) * tpr;
+            int g = sub;
+            const float4* q = a.partials + r + static_cast<size_t>(g) * a.R;
+            for (; g + 3 * tpr < a.n_groups; g += 4 * tpr, q += 4 * stride) {
+                const float4 v0 = __ldg(q), v1 = __ldg(q + stride), v2 = __ldg(q + 2 * stride),
+                             v3 = __ldg(q + 3 * stride);
+                acc = partial_merge(acc, unpack(v0));
+                acc = partial_merge(acc, unpack(v1));
+                acc = partial_merge(acc, unpack(v2));
+                acc = partial_merge(acc, unpack(v3));
+            }
+            for (; g < a.n_groups; g += tpr, q += stride) acc = partial_merge(acc, unpack(__ldg(q)));
+        }
+        for (int off = 1; off < tpr; off <<= 1) {
+            const Partial o = shfl_xor_partial(acc, off);
+            acc = (sub & off) ? partial_merge(o, acc) : partial_merge(acc, o);
         }
         const float s = acc.s;
         const float conf = 1.0f / s;
         float H = kLn2 * (log2f(s) - acc.u / s);
-        if (act && !(isfinite(s) && isfinite(acc.u) && isfinite(acc.mx) && s >= 1.0f - 1e-3f))
-            flag_status(a.status, DG_ST_NONFINITE);
         H = fmaxf(H, 0.0f);
-        if (act) {
+        if (act && sub == 0) {
+            if (!(isfinite(s) && isfinite(acc.u) && isfinite(acc.mx) && s >= 1.0f - 1e-3f))
+                flag_status(a.status, DG_ST_NONFINITE);
             if (a.argmax) a.argmax[r] = acc.idx;
             if (a.conf) a.conf[r] = conf;
             if (a.entropy) a.entropy[r] = H;
@@ -74,11 +91,19 @@ __global__ void select_kernel(const SelectArgs a) {
                 if (a.trace_entropy) a.trace_entropy[tr] = H;
             }
         }
-        // ---- mean entropy of the canvas ----
-        const float sumH = block_reduce_sum_pow2(sh_red, act ? H : 0.0f);
-        const float meanH = sumH / static_cast<float>(a.S);
-        if (j == 0 && a.mean_entropy) a.mean_entropy[b] = meanH;
-        if (j == 0 && a.trace_mean_entropy && a.ctl) a.trace_mean_entropy[p * a.B + b] = meanH;
+        // ---- mean entropy of the canvas: fixed-order pairwise tree over the slots ----
+        if (sub == 0) {
+            sh_red[j] = act ? H : 0.0f;
+            sh_conf[j] = act ? conf : 0.0f;
+        }
+        __syncthreads();
+        for (int off = rows_pow2 >> 1; off > 0; off >>= 1) {
+            if (threadIdx.x < off) sh_red[threadIdx.x] += sh_red[threadIdx.x + off];
+            __syncthreads();
+        }
+        const float meanH = sh_red[0] / static_cast<float>(a.S);
+        if (threadIdx.x == 0 && a.mean_entropy) a.mean_entropy[b] = meanH;
+        if (threadIdx.x == 0 && a.trace_mean_entropy && a.ctl) a.trace_mean_entropy[p * a.B + b] = meanH;
 
         if (a.canvas_out) {
             // ---- keep the K most confident slots, re-draw the rest ----
@@ -90,28 +115,30 @@ __global__ void select_kernel(const SelectArgs a) {
             else
                 K = a.keep_k;
             K = K < 0 ? 0 : (K > a.S ? a.S : K);
-            sh_conf[j] = act ? conf : 0.0f;
-            __syncthreads();
             int rank = 0;
-            for (int i = 0; i < a.S; ++i) {
+            for (int i = sub; i < a.S; i += tpr) {
                 const float ci = sh_conf[i];
                 rank += (ci > conf) || (ci == conf && i < j);
             }
+            for (int off = 1; off < tpr; off <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, off);
             const bool kp = act && rank < K;
             int old = 0, nw = 0;
             if (act) {
                 old = a.canvas_in[r];
-                if (old < 0 || old >= a.V) flag_status(a.status, DG_ST_BAD_TOKEN);
                 nw = kp ? acc.idx
                         : static_cast<int>(draw_key(a.seed, static_cast<uint32_t>(p),
                                                     static_cast<uint64_t>(r)) %
                                            static_cast<uint64_t>(a.V));
+            }
+            __syncthreads();  // every slot read its old token before any slot writes (in place)
+            if (act && sub == 0) {
+                if (old < 0 || old >= a.V) flag_status(a.status, DG_ST_BAD_TOKEN);
                 if (a.trace_canvas && a.ctl) a.trace_canvas[static_cast<size_t>(p) * a.R + r] = old;
                 a.canvas_out[r] = nw;
                 if (a.kept) a.kept[r] = kp ? 1 : 0;
             }
             const int changed = __syncthreads_or(act && nw != old);
-            if (j == 0 && a.state && a.has_rule) {
+            if (threadIdx.x == 0 && a.state && a.has_rule) {
                 dg_canvas_state st = a.state[b];
                 st.stable = changed ? 0 : st.stable + 1;
                 const bool ent = meanH < a.rule.entropy_threshold;
@@ -134,7 +161,7 @@ __global__ void select_kernel(const SelectArgs a) {
     // ---- loop mode: the last CTA of the pass advances the pass and sets the graph condition ----
     if (a.ctl) {
         __syncthreads();
-        if (j == 0) {
+        if (threadIdx.x == 0) {
             __threadfence();
             const unsigned t = atomicAdd(&a.ctl->ticket, 1u);
             if (t == static_cast<unsigned>(a.B) - 1u) {
@@ -298,8 +325,10 @@ int pow2_at_least(int x) {
 }  // namespace
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream) {
-    const int T = pow2_at_least(a.S);
-    select_kernel<<<a.B, T, 2 * T * sizeof(float), stream>>>(a);
+    const int rows = pow2_at_least(a.S);      // 32 .. 1024
+    int tpr = 1024 / rows;
+    if (tpr > 8) tpr = 8;
+    select_kernel<<<a.B, rows * tpr, 2 * rows * sizeof(float), stream>>>(a, tpr);
     return cudaGetLastError();
 }
 
