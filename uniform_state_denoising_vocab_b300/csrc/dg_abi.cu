@@ -29,6 +29,32 @@ HeadPlan plan_head(int R, int V, int d, int BM, int BN, int slots) {
     p.n_groups = g;
     p.units = p.MB * g;
     p.grid = p.units < slots ? p.units : slots;
+    p.pair = 0;
+    return p;
+}
+
+HeadPlan plan_head_pair(int R, int V, int d, int max_pairs) {
+    HeadPlan p{};
+    p.R = R;
+    p.V = V;
+    p.d = d;
+    p.BM = 2 * kTcBM;
+    p.BN = kTcBN;
+    p.MB = (R + p.BM - 1) / p.BM;
+    p.NT = (V + p.BN - 1) / p.BN;
+    int a = p.MB, b = max_pairs;
+    while (b) {
+        const int t = a % b;
+        a = b;
+        b = t;
+    }
+    int g = max_pairs / a;  // a = gcd(MB, pairs): MB * g = lcm(MB, pairs)
+    if (g > p.NT) g = p.NT;
+    if (g < 1) g = 1;
+    p.n_groups = g;
+    p.units = p.MB * g;
+    p.grid = p.units < max_pairs ? p.units : max_pairs;
+    p.pair = 1;
     return p;
 }
 
@@ -38,6 +64,7 @@ enum Path { PATH_SIMT = 0, PATH_TC_BF16 = 1, PATH_TC_E4M3 = 2, PATH_TC_E4M3_QUAN
 
 struct DeviceInfo {
     int sms = 0;
+    int pairs = 0;  // resident clusters of the CTA-pair head kernel
     bool ok = false;
 };
 
@@ -56,6 +83,7 @@ int device_info(DeviceInfo* out) {
             return DG_ERR_CUDA;
         if (major != 10 || minor != 3) return DG_ERR_UNSUPPORTED;
         cache[dev].sms = sms;
+        cache[dev].pairs = head_tc2_max_pairs();
         cache[dev].ok = true;
     }
     *out = cache[dev];
@@ -99,13 +127,15 @@ int classify(const dg_head_desc* d) {
 
 struct Layout {
     HeadPlan plan;
-    size_t off_partials, off_ctl, off_qh, off_sch, total;
+    size_t off_partials, off_ctl, off_tickets, off_stats, off_qh, off_sch, total;
 };
 
 int layout_for(const dg_head_desc* d, int path, const DeviceInfo& di, Layout* L) {
     const int R = d->B * d->S;
     if (path == PATH_SIMT)
         L->plan = plan_head(R, d->V, d->d, kSimtBM, kSimtBN, di.sms * 8);
+    else if (R > kTcBM && di.pairs > 0)
+        L->plan = plan_head_pair(R, d->V, d->d, di.pairs);  // 256-row tiles over CTA pairs
     else
         L->plan = plan_head(R, d->V, d->d, kTcBM, kTcBN, di.sms);
     size_t off = 0;
@@ -113,6 +143,10 @@ int layout_for(const dg_head_desc* d, int path, const DeviceInfo& di, Layout* L)
     off = up256(off + static_cast<size_t>(L->plan.n_groups) * R * 16);
     L->off_ctl = off;
     off = up256(off + sizeof(LoopCtl));
+    L->off_tickets = off;
+    off = up256(off + static_cast<size_t>(d->B) * 4);
+    L->off_stats = off;  // argmax, conf, entropy [R] each, for outputs the caller leaves NULL
+    off = up256(off + static_cast<size_t>(R) * 12);
     L->off_qh = off;
     L->off_sch = off;
     if (path == PATH_TC_E4M3_QUANT) {
@@ -190,6 +224,8 @@ cudaError_t launch_head_only(const dg_head_desc* d, const Prepared& P, uint8_t* 
     a.n_groups = pl.n_groups;
     a.crow_base = d->inv_temp * 1.4426950408889634f;
     a.partials = reinterpret_cast<float4*>(ws + P.L.off_partials);
+    a.tickets = reinterpret_cast<uint32_t*>(ws + P.L.off_tickets);
+    a.n_tickets = d->B;
     a.status = status;
     a.w_scale = d->w_scale;
     a.h_scale = d->h_scale;
@@ -201,10 +237,10 @@ cudaError_t launch_head_only(const dg_head_desc* d, const Prepared& P, uint8_t* 
                                 pl.grid, stream);
     case PATH_TC_BF16:
         a.num_kb = (pl.d + 63) / 64;
-        return launch_head_tc(0, d->h, d->w, a, pl.grid, stream);
+        return launch_head_tc(0, d->h, d->w, a, pl, stream);
     case PATH_TC_E4M3:
         a.num_kb = (pl.d + 127) / 128;
-        return launch_head_tc(1, d->h, d->w, a, pl.grid, stream);
+        return launch_head_tc(1, d->h, d->w, a, pl, stream);
     case PATH_TC_E4M3_QUANT:
     case -PATH_TC_E4M3_QUANT: {
         uint8_t* qh = ws + P.L.off_qh;
@@ -216,7 +252,7 @@ cudaError_t launch_head_only(const dg_head_desc* d, const Prepared& P, uint8_t* 
         }
         a.h_scale = sch;
         a.num_kb = (pl.d + 127) / 128;
-        return launch_head_tc(1, qh, d->w, a, pl.grid, stream);
+        return launch_head_tc(1, qh, d->w, a, pl, stream);
     }
     }
     return cudaErrorInvalidValue;
@@ -226,6 +262,7 @@ SelectArgs base_select(const dg_head_desc* d, const Prepared& P, uint8_t* ws, ui
     SelectArgs s{};
     s.partials = reinterpret_cast<const float4*>(ws + P.L.off_partials);
     s.n_groups = P.L.plan.n_groups;
+    s.tickets = reinterpret_cast<uint32_t*>(ws + P.L.off_tickets);
     s.R = d->B * d->S;
     s.S = d->S;
     s.B = d->B;
@@ -233,6 +270,16 @@ SelectArgs base_select(const dg_head_desc* d, const Prepared& P, uint8_t* ws, ui
     s.keep_k0 = -1;
     s.status = status;
     return s;
+}
+
+// Point the per-row statistics at the caller's arrays, or at workspace scratch where NULL.
+void set_stats(SelectArgs* s, const Prepared& P, uint8_t* ws, int32_t* argmax, float* conf,
+               float* entropy) {
+    const size_t R = static_cast<size_t>(s->R);
+    uint8_t* st = ws + P.L.off_stats;
+    s->argmax = argmax ? argmax : reinterpret_cast<int32_t*>(st);
+    s->conf = conf ? conf : reinterpret_cast<float*>(st + 4 * R);
+    s->entropy = entropy ? entropy : reinterpret_cast<float*>(st + 8 * R);
 }
 
 }  // namespace
@@ -289,9 +336,7 @@ int dg_canvas_stats(const dg_head_desc* desc, int32_t* argmax, float* conf, floa
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (enqueue_head(desc, P, ws, status, st) != cudaSuccess) return DG_ERR_CUDA;
     SelectArgs s = base_select(desc, P, ws, status);
-    s.argmax = argmax;
-    s.conf = conf;
-    s.entropy = entropy;
+    set_stats(&s, P, ws, argmax, conf, entropy);
     s.mean_entropy = mean_entropy;
     if (launch_select(s, st) != cudaSuccess) return DG_ERR_CUDA;
     return DG_OK;
@@ -314,9 +359,7 @@ int dg_canvas_step(const dg_head_desc* desc, const int32_t* canvas_in, int32_t* 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (enqueue_head(desc, P, ws, status, st) != cudaSuccess) return DG_ERR_CUDA;
     SelectArgs s = base_select(desc, P, ws, status);
-    s.argmax = argmax;
-    s.conf = conf;
-    s.entropy = entropy;
+    set_stats(&s, P, ws, argmax, conf, entropy);
     s.mean_entropy = mean_entropy;
     s.kept = kept;
     s.canvas_in = canvas_in;
@@ -442,9 +485,7 @@ int build_loop_graph(LoopEntry* E, const Prepared& P) {
     if (rc == DG_OK && enqueue_head(d, P, ws, k.status, cs) != cudaSuccess) rc = DG_ERR_CUDA;
     if (rc == DG_OK) {
         SelectArgs s = base_select(d, P, ws, k.status);
-        s.argmax = k.argmax;
-        s.conf = k.conf;
-        s.entropy = k.entropy;
+        set_stats(&s, P, ws, k.argmax, k.conf, k.entropy);
         s.canvas_in = k.canvas;
         s.canvas_out = k.canvas;
         s.keep_k0 = k.params.keep_k0;

@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(BM)
     __shared__ __align__(16) float ws[BN][KC];
     const int t = threadIdx.x;
     const int units = args.MB * args.n_groups;
+    zero_tickets(args);
+    grid_launch_dependents();
     for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
         const int mb = unit % args.MB, grp = unit / args.MB;
         const int row = mb * BM + t;
@@ -74,7 +76,8 @@ __global__ void __launch_bounds__(BM)
                     row_state_update<true>(st, v, crow, nb * BN + c * 32, valid);
             }
         }
-        if (row_ok) args.partials[static_cast<size_t>(grp) * args.R + row] = pack(row_state_partial(st));
+        if (row_ok)
+            args.partials[static_cast<size_t>(row) * args.n_groups + grp] = pack(row_state_partial(st));
     }
 }
 

@@ -23,6 +23,7 @@
 
 #include "dg_common.cuh"
 #include "dg_internal.h"
+#include "dg_head_epi.cuh"
 #include "dg_ptx.cuh"
 
 namespace dg {
@@ -68,6 +69,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int units = args.MB * args.n_groups;
+    zero_tickets(args);
+    grid_launch_dependents();
     constexpr int KB_ELEMS = (KIND == 0) ? 64 : 128;  // elements per 128-byte K slice
 
     if (threadIdx.x == 0) {
@@ -100,7 +103,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_h = policy_evict_last();
             uint32_t stage = 0, phase = 0, issued = 0;
-            uint32_t last_parity[STAGES];
+            uint32_t parity_bits = 0;  // bit s: parity of the last phase issued on stage s
             bool ok = true;
             for (int unit = blockIdx.x; unit < units && ok; unit += gridDim.x) {
                 const int mb = unit % args.MB, grp = unit / args.MB;
@@ -116,7 +119,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                     &ctl->full[stage], pol_h);
                         tma_load_2d(sB + stage * B_BYTES, &tmB, kb * KB_ELEMS, nb * BN,
                                     &ctl->full[stage], pol_w);
-                        last_parity[stage] = phase;
+                        parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
                         ++issued;
                         if (++stage == STAGES) {
                             stage = 0;
@@ -129,7 +132,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t n = issued < STAGES ? issued : STAGES;
             for (uint32_t i = 0; i < n; ++i) {
                 const uint32_t s = (stage + STAGES - 1 - i) % STAGES;
-                if (!mbar_wait(&ctl->full[s], last_parity[s])) flag_status(args.status, DG_ST_TIMEOUT);
+                if (!mbar_wait(&ctl->full[s], (parity_bits >> s) & 1u)) flag_status(args.status, DG_ST_TIMEOUT);
             }
         }
     } else if (warp == 1) {
@@ -191,46 +194,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int nb = grp; nb < args.NT && ok; nb += args.n_groups, ++tcount) {
                 const uint32_t buf = tcount & 1u, tph = (tcount >> 1) & 1u;
                 const int n_base = nb * BN;
-                if (KIND == 1) {
-                    // Warp-local staging (no cross-warp barrier, so an aborting warp can never
-                    // strand the others): the previous tile's reads finished before this sync.
-                    __syncwarp();
-                    for (int j = lane; j < BN; j += 32) {
-                        const int n = n_base + j;
-                        csc[j] = (n < args.V) ? args.w_scale[n] : 0.f;
-                    }
-                    __syncwarp();
-                }
+                if (KIND == 1) stage_column_scales<BN>(csc, args.w_scale, n_base, args.V, lane);
                 if (!mbar_wait(&ctl->tfull[buf], tph, abort_flag)) {
                     set_abort(ctl, args.status);
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const int valid_tile = args.V - n_base;  // columns of this tile inside the vocab
                 const uint32_t taddr0 = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                         buf * BN;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    float v[32];
-                    __syncwarp();
-                    tmem_ld32(taddr0 + c * 32, v);
-                    if (KIND == 1) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] *= csc[c * 32 + j];
-                    }
-                    const int valid = valid_tile - c * 32;
-                    if (valid >= 32)
-                        row_state_update<false>(st, v, crow, n_base + c * 32, 32);
-                    else if (valid > 0)
-                        row_state_update<true>(st, v, crow, n_base + c * 32, valid);
-                }
+                drain_tile<KIND, BN>(st, taddr0, csc, crow, n_base, args.V - n_base);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
             }
             if (ok && row < args.R)
-                args.partials[static_cast<size_t>(grp) * args.R + row] = pack(row_state_partial(st));
+                args.partials[static_cast<size_t>(row) * args.n_groups + grp] =
+                    pack(row_state_partial(st));
         }
     }
 
@@ -281,12 +261,14 @@ bool make_map(CUtensorMap* m, const void* base, int elem_bytes, int rows, int co
 
 }  // namespace
 
-cudaError_t launch_head_tc(int kind, const void* h, const void* w, const HeadArgs& args, int grid,
-                           cudaStream_t stream) {
+cudaError_t launch_head_tc(int kind, const void* h, const void* w, const HeadArgs& args,
+                           const HeadPlan& plan, cudaStream_t stream) {
     const int eb = kind == 0 ? 2 : 1;
     CUtensorMap ma, mb;
-    if (!make_map(&ma, h, eb, args.R, args.d, BM) || !make_map(&mb, w, eb, args.V, args.d, BN))
+    if (!make_map(&ma, h, eb, args.R, args.d, BM) ||
+        !make_map(&mb, w, eb, args.V, args.d, plan.pair ? BN / 2 : BN))
         return cudaErrorInvalidValue;
+    if (plan.pair) return launch_head_tc2(kind, ma, mb, args, plan.grid, stream);
     static bool attr_set[2] = {false, false};
     if (kind == 0) {
         if (!attr_set[0]) {
@@ -296,7 +278,7 @@ cudaError_t launch_head_tc(int kind, const void* h, const void* w, const HeadArg
             if (e != cudaSuccess) return e;
             attr_set[0] = true;
         }
-        head_tc_kernel<0><<<grid, kTcThreads, SMEM_BYTES, stream>>>(ma, mb, args);
+        head_tc_kernel<0><<<plan.grid, kTcThreads, SMEM_BYTES, stream>>>(ma, mb, args);
     } else {
         if (!attr_set[1]) {
             cudaError_t e = cudaFuncSetAttribute(head_tc_kernel<1>,
@@ -305,7 +287,7 @@ cudaError_t launch_head_tc(int kind, const void* h, const void* w, const HeadArg
             if (e != cudaSuccess) return e;
             attr_set[1] = true;
         }
-        head_tc_kernel<1><<<grid, kTcThreads, SMEM_BYTES, stream>>>(ma, mb, args);
+        head_tc_kernel<1><<<plan.grid, kTcThreads, SMEM_BYTES, stream>>>(ma, mb, args);
     }
     return cudaGetLastError();
 }

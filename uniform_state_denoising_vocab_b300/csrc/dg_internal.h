@@ -14,6 +14,7 @@ namespace dg {
 constexpr int kTcBM = 128;
 constexpr int kTcBN = 256;
 constexpr int kTcStages = 4;
+constexpr int kTc2Stages = 6;    // pair kernel: 32 KB stages (128 h rows + 128 W rows)
 constexpr int kTcThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 // Geometry of the fp32 CUDA-core head.
 constexpr int kSimtBM = 128;
@@ -22,13 +23,17 @@ constexpr int kSimtBN = 64;
 // Work decomposition of a head pass: MB row blocks x NT vocabulary tiles, each row block split
 // into n_groups vocabulary groups (group g takes tiles g, g + n_groups, ...). A (row block,
 // group) unit writes one Partial per row into partials[g * R + row].
+// For the CTA-pair kernel (pair = 1) a row block is 256 rows and `grid` counts pairs.
 struct HeadPlan {
     int R, V, d;
     int BM, BN;
     int MB, NT, n_groups, units, grid;
+    int pair;
 };
 
 HeadPlan plan_head(int R, int V, int d, int BM, int BN, int num_sms);
+// Pair plan: groups chosen so that units = lcm(MB, pairs) spread evenly over the pairs.
+HeadPlan plan_head_pair(int R, int V, int d, int max_pairs);
 
 struct HeadArgs {
     int R, V, d;
@@ -36,13 +41,33 @@ struct HeadArgs {
     float crow_base;          // inv_temp * log2(e)
     const float* h_scale;     // [R] or null
     const float* w_scale;     // [V] or null
-    float4* partials;         // [n_groups][R]
+    float4* partials;         // [R][n_groups]: the partials of one row are contiguous
+    uint32_t* tickets;        // [n_tickets] per-canvas arrival counters of the merge, zeroed here
+    int n_tickets;
     uint32_t* status;         // sticky status word or null
 };
 
+// The merge kernel's per-canvas arrival counters start every pass at zero: each head launch
+// (which precedes the merge in stream order) clears them.
+__device__ __forceinline__ void zero_tickets(const HeadArgs& a) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.n_tickets; i += gridDim.x * blockDim.x)
+        a.tickets[i] = 0;
+}
+
+// Allow the dependent launch (the merge kernel) to be scheduled now; it still waits for this
+// grid's completion before reading anything.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Tensor-core head (bf16: kind = 0, e4m3: kind = 1). h and w are device row-major matrices.
+// Runs the CTA-pair kernel when plan.pair, else the single-CTA kernel.
 cudaError_t launch_head_tc(int kind, const void* h, const void* w, const HeadArgs& args,
-                           int grid, cudaStream_t stream);
+                           const HeadPlan& plan, cudaStream_t stream);
+cudaError_t launch_head_tc2(int kind, const CUtensorMap& ma, const CUtensorMap& mb,
+                            const HeadArgs& args, int n_pairs, cudaStream_t stream);
+// Resident clusters of the pair kernel on the current device (0 if it cannot run).
+int head_tc2_max_pairs();
 // fp32 CUDA-core head.
 cudaError_t launch_head_simt(const float* h, const float* w, const HeadArgs& args, int grid,
                              cudaStream_t stream);
@@ -56,13 +81,13 @@ struct LoopCtl {
 };
 
 struct SelectArgs {
-    const float4* partials;
+    const float4* partials;           // [R][n_groups]
     int n_groups, R, S, B, V;
-    float inv_crow_base;              // 1 / (inv_temp * log2 e): unused, kept for clarity
-    int32_t* argmax;                  // outputs, each may be null
+    uint32_t* tickets;                // [B] arrival counters (zero on entry, left zero on exit)
+    int32_t* argmax;                  // per-row statistics: caller's arrays or workspace scratch
     float* conf;
     float* entropy;
-    float* mean_entropy;
+    float* mean_entropy;              // optional [B]
     uint8_t* kept;
     const int32_t* canvas_in;         // null: statistics only
     int32_t* canvas_out;

@@ -1,6 +1,7 @@
 // dg_sampler.cu -- the per-canvas part of a pass and the loop plumbing:
-//   select_kernel   merge the vocabulary-group partials of every slot into argmax, confidence
-//                   and entropy; per canvas: mean entropy (fixed-order tree), rank slots by
+//   merge_select    merge the vocabulary-group partials of every slot into argmax, confidence
+//                   and entropy (one warp per slot); then, in the last CTA of each canvas to
+//                   finish: mean entropy (fixed-order tree), rank slots by
 //                   (confidence desc, slot asc), keep the top K at their argmax, re-draw the
 //                   rest uniformly with the SplitMix64 counter key, and apply the stop rules.
 //                   "Each pass, the model predicts every slot at once, keeps the ones it's most
@@ -33,57 +34,150 @@ __device__ __forceinline__ Partial shfl_xor_partial(const Partial& p, int off) {
     return q;
 }
 
-// One CTA per canvas, `tpr` (1..8, a power of two) consecutive threads per slot row:
-// the threads of a row merge disjoint, strided subsets of the vocabulary-group partials with
-// their loads batched, then combine them with a fixed xor butterfly (lower sub-lane first), so
-// every run merges in the same order.
-__global__ void __launch_bounds__(1024) select_kernel(const SelectArgs a, int tpr) {
-    extern __shared__ float sh[];  // [2 * rows_pow2]: reduction scratch, confidences
-    const int rows_pow2 = blockDim.x / tpr;
-    float* sh_red = sh;
-    float* sh_conf = sh + rows_pow2;
-    const int b = blockIdx.x;
-    const int j = threadIdx.x / tpr;       // slot
-    const int sub = threadIdx.x % tpr;
-    const bool act = j < a.S;
-    const int r = b * a.S + j;
-    const int p = a.ctl ? a.ctl->pass : static_cast<int>(a.pass);
+// Wait until the grid this launch depends on (the head kernel, when launched as a programmatic
+// dependent) has completed and its memory is visible. A no-op for a normal launch.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
-    const bool frozen = a.state != nullptr && a.state[b].done != 0;
+constexpr int kMergeWarps = 16;            // slot rows merged per CTA (one warp per row)
+constexpr int kMergeThreads = kMergeWarps * 32;
+
+// Per-canvas part of a pass, run by the last CTA of the canvas to finish its rows:
+// mean entropy (fixed-order pairwise tree over the slots), rank by (confidence desc, slot asc),
+// keep the top K at their argmax, re-draw the rest with the counter key, stop rules.
+__device__ void canvas_tail(const SelectArgs& a, int b, int p, bool frozen, float* sh_red,
+                            float* sh_conf, int rows_pow2) {
+    const int tid = threadIdx.x;
+    const int base = b * a.S;
     if (frozen) {
-        if (act && sub == 0 && a.canvas_out && a.canvas_out != a.canvas_in)
-            a.canvas_out[r] = a.canvas_in[r];
-    } else {
-        // ---- merge the partials of this row ----
-        Partial acc = partial_empty();
-        if (act) {
-            const size_t stride = static_cast<size_t>(a.R) * tpr;
-            int g = sub;
-            const float4* q = a.partials + r + static_cast<size_t>(g) * a.R;
-            for (; g + 3 * tpr < a.n_groups; g += 4 * tpr, q += 4 * stride) {
-                const float4 v0 = __ldg(q), v1 = __ldg(q + stride), v2 = __ldg(q + 2 * stride),
-                             v3 = __ldg(q + 3 * stride);
-                acc = partial_merge(acc, unpack(v0));
-                acc = partial_merge(acc, unpack(v1));
-                acc = partial_merge(acc, unpack(v2));
-                acc = partial_merge(acc, unpack(v3));
+        if (a.canvas_out && a.canvas_out != a.canvas_in)
+            for (int j = tid; j < a.S; j += blockDim.x) a.canvas_out[base + j] = a.canvas_in[base + j];
+        return;
+    }
+    // statistics of the canvas's rows, written by every CTA of the canvas (L2, not L1)
+    for (int j = tid; j < rows_pow2; j += blockDim.x) {
+        sh_red[j] = j < a.S ? __ldcg(a.entropy + base + j) : 0.0f;
+        sh_conf[j] = j < a.S ? __ldcg(a.conf + base + j) : 0.0f;
+    }
+    __syncthreads();
+    for (int off = rows_pow2 >> 1; off > 0; off >>= 1) {
+        for (int j = tid; j < off; j += blockDim.x) sh_red[j] += sh_red[j + off];
+        __syncthreads();
+    }
+    const float meanH = sh_red[0] / static_cast<float>(a.S);
+    if (tid == 0 && a.mean_entropy) a.mean_entropy[b] = meanH;
+    if (tid == 0 && a.trace_mean_entropy && a.ctl) a.trace_mean_entropy[p * a.B + b] = meanH;
+    if (!a.canvas_out) return;
+
+    long long K;
+    if (a.keep_sched)
+        K = a.keep_sched[p];
+    else if (a.keep_k0 >= 0)
+        K = static_cast<long long>(a.keep_k0) * (p + 1);
+    else
+        K = a.keep_k;
+    K = K < 0 ? 0 : (K > a.S ? a.S : K);
+
+    // tpr threads per slot (a power of two dividing 32) split the rank count
+    int tpr = static_cast<int>(blockDim.x) / rows_pow2;
+    tpr = tpr < 1 ? 1 : (tpr > 8 ? 8 : tpr);
+    const int sub = tid % tpr;
+    const int slots_per_round = static_cast<int>(blockDim.x) / tpr;
+    int changed = 0;
+    for (int j0 = 0; j0 < rows_pow2; j0 += slots_per_round) {
+        const int j = j0 + tid / tpr;
+        const bool act = j < a.S;
+        const float cj = act ? sh_conf[j] : 0.0f;
+        int rank = 0;
+        if (act)
+            for (int i = sub; i < a.S; i += tpr) {
+                const float ci = sh_conf[i];
+                rank += (ci > cj) || (ci == cj && i < j);
             }
-            for (; g < a.n_groups; g += tpr, q += stride) acc = partial_merge(acc, unpack(__ldg(q)));
-        }
-        for (int off = 1; off < tpr; off <<= 1) {
-            const Partial o = shfl_xor_partial(acc, off);
-            acc = (sub & off) ? partial_merge(o, acc) : partial_merge(acc, o);
-        }
-        const float s = acc.s;
-        const float conf = 1.0f / s;
-        float H = kLn2 * (log2f(s) - acc.u / s);
-        H = fmaxf(H, 0.0f);
+        for (int off = 1; off < tpr; off <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, off);
         if (act && sub == 0) {
+            const int r = base + j;
+            const bool kp = rank < K;
+            const int old = a.canvas_in[r];
+            const int nw = kp ? __ldcg(a.argmax + r)
+                              : static_cast<int>(draw_key(a.seed, static_cast<uint32_t>(p),
+                                                          static_cast<uint64_t>(r)) %
+                                                 static_cast<uint64_t>(a.V));
+            if (old < 0 || old >= a.V) flag_status(a.status, DG_ST_BAD_TOKEN);
+            if (a.trace_canvas && a.ctl) a.trace_canvas[static_cast<size_t>(p) * a.R + r] = old;
+            a.canvas_out[r] = nw;
+            if (a.kept) a.kept[r] = kp ? 1 : 0;
+            changed |= (nw != old);
+        }
+    }
+    changed = __syncthreads_or(changed);
+    if (tid == 0 && a.state && a.has_rule) {
+        dg_canvas_state st = a.state[b];
+        st.stable = changed ? 0 : st.stable + 1;
+        const bool ent = meanH < a.rule.entropy_threshold;
+        const bool stb = st.stable >= a.rule.stable_passes;
+        const bool cap = p + 1 >= a.rule.max_passes;
+        const bool stop = (a.rule.stop_mode == DG_STOP_AND ? (ent && stb) : (ent || stb)) || cap;
+        st.mean_entropy = meanH;
+        st.last_pass = p;
+        if (stop) {
+            st.done = 1;
+            st.passes = p + 1;
+            st.reason = (ent ? DG_REASON_ENTROPY : 0) | (stb ? DG_REASON_STABLE : 0) |
+                        (cap ? DG_REASON_CAP : 0);
+        }
+        a.state[b] = st;
+    }
+}
+
+// Grid: B x ceil(S / kMergeWarps) CTAs of kMergeThreads. Warp w of CTA (b, x) merges the
+// vocabulary-group partials of slot x * kMergeWarps + w of canvas b: lane l takes groups
+// l, l + 32, ... in increasing order, then the lanes combine with a fixed xor butterfly (lower
+// lane first), so every run merges in the same order and all lanes end with the same result.
+// The last CTA of a canvas to arrive (arrival counter in a.tickets) runs the canvas tail; in
+// loop mode the last canvas tail of the pass advances the pass and sets the graph condition.
+__global__ void __launch_bounds__(kMergeThreads) merge_select_kernel(const SelectArgs a,
+                                                                      int ctas_per_canvas) {
+    extern __shared__ float sh[];  // [2 * rows_pow2]: entropy tree, confidences
+    __shared__ int sh_last;
+    grid_dependency_wait();
+    const int rows_pow2 = max(32, 1 << (32 - __clz(a.S - 1)));
+    const int b = blockIdx.x / ctas_per_canvas;
+    const int x = blockIdx.x % ctas_per_canvas;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int j = x * kMergeWarps + warp;
+    const int p = a.ctl ? a.ctl->pass : static_cast<int>(a.pass);
+    const bool frozen = a.state != nullptr && a.state[b].done != 0;
+
+    if (!frozen && j < a.S) {
+        const int r = b * a.S + j;
+        const float4* q = a.partials + static_cast<size_t>(r) * a.n_groups;
+        Partial acc = partial_empty();
+        int g = lane;
+        for (; g + 96 < a.n_groups; g += 128) {
+            const float4 v0 = __ldcg(q + g), v1 = __ldcg(q + g + 32), v2 = __ldcg(q + g + 64),
+                         v3 = __ldcg(q + g + 96);
+            acc = partial_merge(acc, unpack(v0));
+            acc = partial_merge(acc, unpack(v1));
+            acc = partial_merge(acc, unpack(v2));
+            acc = partial_merge(acc, unpack(v3));
+        }
+        for (; g < a.n_groups; g += 32) acc = partial_merge(acc, unpack(__ldcg(q + g)));
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const Partial o = shfl_xor_partial(acc, off);
+            acc = (lane & off) ? partial_merge(o, acc) : partial_merge(acc, o);
+        }
+        if (lane == 0) {
+            const float s = acc.s;
+            const float conf = 1.0f / s;
+            const float H = fmaxf(kLn2 * (log2f(s) - acc.u / s), 0.0f);
             if (!(isfinite(s) && isfinite(acc.u) && isfinite(acc.mx) && s >= 1.0f - 1e-3f))
                 flag_status(a.status, DG_ST_NONFINITE);
-            if (a.argmax) a.argmax[r] = acc.idx;
-            if (a.conf) a.conf[r] = conf;
-            if (a.entropy) a.entropy[r] = H;
+            a.argmax[r] = acc.idx;
+            a.conf[r] = conf;
+            a.entropy[r] = H;
             if (a.ctl) {
                 const size_t tr = static_cast<size_t>(p) * a.R + r;
                 if (a.trace_argmax) a.trace_argmax[tr] = acc.idx;
@@ -91,74 +185,24 @@ __global__ void __launch_bounds__(1024) select_kernel(const SelectArgs a, int tp
                 if (a.trace_entropy) a.trace_entropy[tr] = H;
             }
         }
-        // ---- mean entropy of the canvas: fixed-order pairwise tree over the slots ----
-        if (sub == 0) {
-            sh_red[j] = act ? H : 0.0f;
-            sh_conf[j] = act ? conf : 0.0f;
-        }
-        __syncthreads();
-        for (int off = rows_pow2 >> 1; off > 0; off >>= 1) {
-            if (threadIdx.x < off) sh_red[threadIdx.x] += sh_red[threadIdx.x + off];
-            __syncthreads();
-        }
-        const float meanH = sh_red[0] / static_cast<float>(a.S);
-        if (threadIdx.x == 0 && a.mean_entropy) a.mean_entropy[b] = meanH;
-        if (threadIdx.x == 0 && a.trace_mean_entropy && a.ctl) a.trace_mean_entropy[p * a.B + b] = meanH;
-
-        if (a.canvas_out) {
-            // ---- keep the K most confident slots, re-draw the rest ----
-            long long K;
-            if (a.keep_sched)
-                K = a.keep_sched[p];
-            else if (a.keep_k0 >= 0)
-                K = static_cast<long long>(a.keep_k0) * (p + 1);
-            else
-                K = a.keep_k;
-            K = K < 0 ? 0 : (K > a.S ? a.S : K);
-            int rank = 0;
-            for (int i = sub; i < a.S; i += tpr) {
-                const float ci = sh_conf[i];
-                rank += (ci > conf) || (ci == conf && i < j);
-            }
-            for (int off = 1; off < tpr; off <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, off);
-            const bool kp = act && rank < K;
-            int old = 0, nw = 0;
-            if (act) {
-                old = a.canvas_in[r];
-                nw = kp ? acc.idx
-                        : static_cast<int>(draw_key(a.seed, static_cast<uint32_t>(p),
-                                                    static_cast<uint64_t>(r)) %
-                                           static_cast<uint64_t>(a.V));
-            }
-            __syncthreads();  // every slot read its old token before any slot writes (in place)
-            if (act && sub == 0) {
-                if (old < 0 || old >= a.V) flag_status(a.status, DG_ST_BAD_TOKEN);
-                if (a.trace_canvas && a.ctl) a.trace_canvas[static_cast<size_t>(p) * a.R + r] = old;
-                a.canvas_out[r] = nw;
-                if (a.kept) a.kept[r] = kp ? 1 : 0;
-            }
-            const int changed = __syncthreads_or(act && nw != old);
-            if (threadIdx.x == 0 && a.state && a.has_rule) {
-                dg_canvas_state st = a.state[b];
-                st.stable = changed ? 0 : st.stable + 1;
-                const bool ent = meanH < a.rule.entropy_threshold;
-                const bool stb = st.stable >= a.rule.stable_passes;
-                const bool cap = p + 1 >= a.rule.max_passes;
-                const bool stop = (a.rule.stop_mode == DG_STOP_AND ? (ent && stb) : (ent || stb)) || cap;
-                st.mean_entropy = meanH;
-                st.last_pass = p;
-                if (stop) {
-                    st.done = 1;
-                    st.passes = p + 1;
-                    st.reason = (ent ? DG_REASON_ENTROPY : 0) | (stb ? DG_REASON_STABLE : 0) |
-                                (cap ? DG_REASON_CAP : 0);
-                }
-                a.state[b] = st;
-            }
-        }
     }
 
-    // ---- loop mode: the last CTA of the pass advances the pass and sets the graph condition ----
+    // arrival: the last CTA of canvas b (in arrival order) sees every row's statistics
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned t = atomicAdd(&a.tickets[b], 1u);
+        sh_last = (t == static_cast<unsigned>(ctas_per_canvas) - 1u);
+        if (sh_last) {
+            a.tickets[b] = 0;  // ready for the next pass
+            __threadfence();
+        }
+    }
+    __syncthreads();
+    if (!sh_last) return;
+    canvas_tail(a, b, p, frozen, sh, sh + rows_pow2, rows_pow2);
+
+    // loop mode: the last canvas tail of the pass advances the pass and sets the graph condition
     if (a.ctl) {
         __syncthreads();
         if (threadIdx.x == 0) {
@@ -325,11 +369,21 @@ int pow2_at_least(int x) {
 }  // namespace
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream) {
-    const int rows = pow2_at_least(a.S);      // 32 .. 1024
-    int tpr = 1024 / rows;
-    if (tpr > 8) tpr = 8;
-    select_kernel<<<a.B, rows * tpr, 2 * rows * sizeof(float), stream>>>(a, tpr);
-    return cudaGetLastError();
+    const int rows = pow2_at_least(a.S);  // 32 .. 1024
+    const int cpc = (a.S + kMergeWarps - 1) / kMergeWarps;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(a.B) * cpc));
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = 2 * rows * sizeof(float);
+    cfg.stream = stream;
+    // Programmatic dependent launch: the merge grid may be scheduled while the head kernel
+    // drains; griddepcontrol.wait at its top orders every read after the head's writes.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, merge_select_kernel, a, cpc);
 }
 
 cudaError_t launch_quant_rows(const uint16_t* h, int R, int d, uint8_t* q, float* scale,
