@@ -162,3 +162,105 @@ def test_loop_rules_on_device(dg):
     torch.cuda.synchronize()
     f = dg.state_fields(r["state"])
     assert f["passes"].tolist() == [1] and f["reason"][0] & dg.REASON_ENTROPY
+
+
+def _run_loop(dg, cfg, x, trace=True):
+    if cfg.precision == "bf16":
+        tw, tws = dev_bf16(x["w"], (cfg.V, cfg.d)), None
+    else:
+        tw, tws = dev_u8(x["w"], (cfg.V, cfg.d)), dev(x["w_scale"])
+    canvas = torch.empty(cfg.R, dtype=torch.int32, device="cuda")
+    res = dg.dg_canvas_loop(tw, canvas, B=cfg.B, S=cfg.S, theta=cfg.theta, y=dev(x["y"]),
+                            w_scale=tws, keep_k0=cfg.keep_k, seed=cfg.seed,
+                            max_passes=cfg.max_passes, stable_passes=cfg.stable_passes,
+                            n_content=cfg.n_content, s_content=cfg.s_content, s_pad=cfg.s_pad,
+                            trace=trace)
+    torch.cuda.synchronize()
+    return res
+
+
+def test_loop_e4m3_v32768_lockstep_and_free_run(dg, orc):
+    """The FP8 loop at a size the oracle runs in full: E4M3 head with per-row scales, bf16 hidden
+    states from the built-in denoiser quantised per row on the device (fused into the denoiser)."""
+    from workloads import WorkloadConfig, make_loop_inputs
+    cfg = WorkloadConfig("loop_e4m3_v32768_d256", "e4m3", 1, 256, 32768, 256, seed=3, mode="loop")
+    x = make_loop_inputs(cfg)
+    res = _run_loop(dg, cfg, x)
+    assert int(res["status"][0]) == 0
+    st = dg.state_fields(res["state"])
+    assert st["done"][0] == 1
+    P, events = _lockstep(dg, orc, res, cfg, x["w"], x["w_scale"], x["y"], "e4m3")
+    den = lambda c, p: orc.synth_denoise(cfg.B, cfg.S, cfg.d, cfg.V, "e4m3", x["w"], x["y"], c, p,
+                                         cfg.n_content, cfg.s_content, cfg.s_pad,
+                                         w_scale=x["w_scale"])
+    ref = orc.loop(cfg.B, cfg.S, cfg.V, cfg.d, "e4m3", x["w"], den, theta=cfg.theta,
+                   stable_passes=cfg.stable_passes, max_passes=cfg.max_passes,
+                   keep_k0=cfg.keep_k, seed=cfg.seed, w_scale=x["w_scale"])
+    print(f"GPU passes {P} reason {int(st['reason'][0])}; oracle passes {ref['passes'][0]} "
+          f"reason {ref['reason'][0]}; near-tie events {events}")
+    if not events:
+        assert P == ref["passes"][0] and int(st["reason"][0]) == ref["reason"][0]
+        assert np.array_equal(host(res["canvas"]), ref["canvas"])
+
+
+def test_loop_e4m3_full_scale_sampled_lockstep(dg, orc):
+    """The FP8 loop at 256 slots x 262144 vocab x d=2816 in the launch configuration the
+    benchmark times. Every pass: the denoiser output for every row against the oracle's
+    denoiser on the GPU's canvas; the statistics of sampled rows against the oracle one by one
+    (on the GPU's own hidden states, quantised by the oracle); and, for every row, the
+    properties that hold at any size: kept = top-K of the GPU's confidences, the new canvas =
+    argmax where kept and the counter hash elsewhere, the mean entropy = mean of the slot
+    entropies, entropy in [0, ln V], confidence in [1/V, 1]."""
+    from workloads import CONFIGS, make_loop_inputs
+    cfg = CONFIGS["loop_e4m3_v262144_d2816"]
+    x = make_loop_inputs(cfg)
+    res = _run_loop(dg, cfg, x)
+    assert int(res["status"][0]) == 0
+    st = dg.state_fields(res["state"])
+    P = int(st["passes"][0])
+    assert st["done"][0] == 1 and 1 <= P <= cfg.max_passes
+    R, S, V, d = cfg.R, cfg.S, cfg.V, cfg.d
+    tc = host(res["trace_canvas"])
+    th = host(res["trace_h"].view(torch.int16)).view(np.uint16)
+    tm = host(res["trace_mean_entropy"])
+    ta, tcf, te = host(res["trace_argmax"]), host(res["trace_conf"]), host(res["trace_entropy"])
+    final = host(res["canvas"])
+    assert np.array_equal(tc[0], orc.draw(cfg.seed, 0xFFFFFFFF, np.arange(R), V))
+    rng = np.random.default_rng(5)
+    stable = 0
+    for p in range(P):
+        c_p = tc[p]
+        c_next = tc[p + 1] if p + 1 < P else final
+        ho = orc.synth_denoise(cfg.B, S, d, V, "e4m3", x["w"], x["y"], c_p, p, cfg.n_content,
+                               cfg.s_content, cfg.s_pad, w_scale=x["w_scale"])
+        vg, vo = _bf16_values(th[p].reshape(-1)).astype(np.float64), _bf16_values(ho).astype(np.float64)
+        assert (np.abs(vg - vo) <= 2.0**-7 * np.maximum(np.abs(vg), np.abs(vo)) + 1e-5).all()
+        rows = np.sort(rng.choice(R, size=6, replace=False))
+        q, sc = orc.quant_rows_e4m3(th[p].reshape(-1), R, d)
+        o = orc.head_stats(R, d, V, "e4m3", q, x["w"], h_scale=sc, w_scale=x["w_scale"], rows=rows)
+        check_stats({"argmax": ta[p], "conf": tcf[p], "entropy": te[p]}, o, TOL["e4m3"], rows=rows)
+        assert (te[p] >= 0).all() and (te[p] <= np.log(V) + 1e-4).all()
+        assert (tcf[p] >= 0.999 / V).all() and (tcf[p] <= 1.0).all()
+        K = min(cfg.keep_k * (p + 1), S)
+        kept = _gpu_kept(tcf[p], S, K).astype(bool)
+        expect = np.where(kept, ta[p], orc.draw(cfg.seed, p, np.arange(R), V))
+        assert np.array_equal(c_next, expect), f"pass {p}: canvas update"
+        assert abs(tm[p][0] - te[p].astype(np.float64).mean()) < 1e-4
+        stable = 0 if np.any(c_next != c_p) else stable + 1
+        stop = tm[p][0] < cfg.theta or stable >= cfg.stable_passes or p + 1 == cfg.max_passes
+        assert stop == (p + 1 == P), f"pass {p}: stop decision"
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 4608), ("e4m3", 8320), ("bf16", 64), ("e4m3", 48)])
+def test_denoiser_row_widths(dg, orc, dtype, d):
+    """One loop pass at hidden sizes on both sides of the vectorised denoiser's register limit
+    (wider rows take the generic kernel): the hidden states within one bf16 ulp of the oracle's
+    denoiser, and the pass's statistics and canvas against the oracle on them."""
+    from workloads import WorkloadConfig, make_loop_inputs
+    cfg = WorkloadConfig(f"loop_{dtype}_v300_d{d}", dtype, 2, 96, 300, d, seed=9, mode="loop",
+                         max_passes=2, n_content=20)
+    x = make_loop_inputs(cfg)
+    res = _run_loop(dg, cfg, x)
+    assert int(res["status"][0]) == 0
+    P, _ = _lockstep(dg, orc, res, cfg, x["w"], x.get("w_scale"), x["y"], dtype)
+    assert P >= 1

@@ -228,12 +228,15 @@ def dg_canvas_loop(w, canvas, *, B: int, S: int, theta: float, y=None, denoise=N
                    seed: int = 0, max_passes: int = 48, stable_passes: int = 2,
                    stop_mode: int = STOP_OR, start_pass: int = 0, init_random: bool = True,
                    state=None, n_content: int = 50, s_content: float = 8.0, s_pad: float = 16.0,
-                   trace: bool = False, workspace=None, status=None, stream=None) -> dict:
+                   trace: bool = False, workspace=None, status=None, outputs: dict | None = None,
+                   stream=None) -> dict:
     """The whole denoising loop on the device (one graph launch, no host synchronisation).
 
     With y given (and denoise None) the built-in synthetic denoiser is used. `denoise`, if
     given, is a Python callable (canvas_ptr, pass_ptr, h_ptr, stream_handle) -> int that must
-    enqueue capturable work on the stream it receives.
+    enqueue capturable work on the stream it receives. `outputs` may hold preallocated
+    argmax/conf/entropy tensors [B*S]; with the same tensors (and the same other arguments) a
+    repeated call reuses the captured graph.
     """
     dev = w.device
     R = B * S
@@ -245,10 +248,15 @@ def dg_canvas_loop(w, canvas, *, B: int, S: int, theta: float, y=None, denoise=N
     if state is None:
         state = new_state(B, dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev) if status is None else status
+    outputs = outputs or {}
     out = {"canvas": canvas, "state": state, "status": st, "h": h_buffer,
-           "argmax": torch.empty(R, dtype=torch.int32, device=dev),
-           "conf": torch.empty(R, dtype=torch.float32, device=dev),
-           "entropy": torch.empty(R, dtype=torch.float32, device=dev)}
+           "argmax": outputs.get("argmax", None), "conf": outputs.get("conf", None),
+           "entropy": outputs.get("entropy", None)}
+    if out["argmax"] is None:
+        out["argmax"] = torch.empty(R, dtype=torch.int32, device=dev)
+    for k in ("conf", "entropy"):
+        if out[k] is None:
+            out[k] = torch.empty(R, dtype=torch.float32, device=dev)
     params = LoopParams(rule=StopRule(max_passes=max_passes, entropy_threshold=theta,
                                       stable_passes=stable_passes, stop_mode=stop_mode),
                         keep_k0=keep_k0, keep_sched=None if keep_sched is None else _ptr(keep_sched).value,

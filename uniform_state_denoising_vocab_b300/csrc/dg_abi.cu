@@ -127,7 +127,7 @@ int classify(const dg_head_desc* d) {
 
 struct Layout {
     HeadPlan plan;
-    size_t off_partials, off_ctl, off_tickets, off_stats, off_qh, off_sch, total;
+    size_t off_partials, off_ctl, off_stats, off_qh, off_sch, total;
 };
 
 int layout_for(const dg_head_desc* d, int path, const DeviceInfo& di, Layout* L) {
@@ -143,8 +143,6 @@ int layout_for(const dg_head_desc* d, int path, const DeviceInfo& di, Layout* L)
     off = up256(off + static_cast<size_t>(L->plan.n_groups) * R * 16);
     L->off_ctl = off;
     off = up256(off + sizeof(LoopCtl));
-    L->off_tickets = off;
-    off = up256(off + static_cast<size_t>(d->B) * 4);
     L->off_stats = off;  // argmax, conf, entropy [R] each, for outputs the caller leaves NULL
     off = up256(off + static_cast<size_t>(R) * 12);
     L->off_qh = off;
@@ -224,8 +222,6 @@ cudaError_t launch_head_only(const dg_head_desc* d, const Prepared& P, uint8_t* 
     a.n_groups = pl.n_groups;
     a.crow_base = d->inv_temp * 1.4426950408889634f;
     a.partials = reinterpret_cast<float4*>(ws + P.L.off_partials);
-    a.tickets = reinterpret_cast<uint32_t*>(ws + P.L.off_tickets);
-    a.n_tickets = d->B;
     a.status = status;
     a.w_scale = d->w_scale;
     a.h_scale = d->h_scale;
@@ -262,7 +258,6 @@ SelectArgs base_select(const dg_head_desc* d, const Prepared& P, uint8_t* ws, ui
     SelectArgs s{};
     s.partials = reinterpret_cast<const float4*>(ws + P.L.off_partials);
     s.n_groups = P.L.plan.n_groups;
-    s.tickets = reinterpret_cast<uint32_t*>(ws + P.L.off_tickets);
     s.R = d->B * d->S;
     s.S = d->S;
     s.B = d->B;
@@ -405,8 +400,9 @@ struct LoopKey {
     void* h_buffer;
     dg_loop_params params;
     dg_denoise_fn fn;
-    void* user;
-    dg_synth_params synth;  // content of `user` when fn is the built-in denoiser
+    void* user;             // NULL for the built-in denoiser: its parameters are compared by value
+    dg_synth_params synth;  // content of `user` when fn is the built-in denoiser (desc = NULL)
+    dg_head_desc synth_desc;  // content of synth.desc
     dg_canvas_state* state;
     int32_t* argmax;
     float* conf;
@@ -431,6 +427,52 @@ unsigned long long g_stamp = 0;
 constexpr size_t kLoopCache = 16;
 
 bool same_key(const LoopKey& a, const LoopKey& b) { return std::memcmp(&a, &b, sizeof(LoopKey)) == 0; }
+
+// Field-wise copies into zeroed storage, so that padding bytes (which the caller may leave
+// uninitialised) never make two equal keys compare different.
+void copy_desc(dg_head_desc* dst, const dg_head_desc& s) {
+    std::memset(dst, 0, sizeof(*dst));
+    dst->B = s.B;
+    dst->S = s.S;
+    dst->d = s.d;
+    dst->V = s.V;
+    dst->h_dtype = s.h_dtype;
+    dst->w_dtype = s.w_dtype;
+    dst->h = s.h;
+    dst->h_scale = s.h_scale;
+    dst->w = s.w;
+    dst->w_scale = s.w_scale;
+    dst->inv_temp = s.inv_temp;
+}
+
+void copy_params(dg_loop_params* dst, const dg_loop_params& s) {
+    std::memset(dst, 0, sizeof(*dst));
+    dst->rule.max_passes = s.rule.max_passes;
+    dst->rule.entropy_threshold = s.rule.entropy_threshold;
+    dst->rule.stable_passes = s.rule.stable_passes;
+    dst->rule.stop_mode = s.rule.stop_mode;
+    dst->keep_k0 = s.keep_k0;
+    dst->keep_sched = s.keep_sched;
+    dst->seed = s.seed;
+    dst->start_pass = s.start_pass;
+    dst->init_random = s.init_random;
+    dst->trace_mean_entropy = s.trace_mean_entropy;
+    dst->trace_canvas = s.trace_canvas;
+    dst->trace_h = s.trace_h;
+    dst->trace_argmax = s.trace_argmax;
+    dst->trace_conf = s.trace_conf;
+    dst->trace_entropy = s.trace_entropy;
+}
+
+void copy_synth(dg_synth_params* dst, const dg_synth_params& s) {
+    std::memset(dst, 0, sizeof(*dst));
+    dst->desc = s.desc;
+    dst->y = s.y;
+    dst->n_content = s.n_content;
+    dst->s_content = s.s_content;
+    dst->s_pad = s.s_pad;
+    dst->status = s.status;
+}
 
 cudaStream_t capture_stream() {
     static std::mutex mu;
@@ -475,14 +517,28 @@ int build_loop_graph(LoopEntry* E, const Prepared& P) {
         return DG_ERR_CUDA;
     }
     int rc = DG_OK;
-    void* user = (k.fn == dg_synth_denoise) ? static_cast<void*>(&E->synth_user) : k.user;
-    if (k.fn(user, k.canvas, &ctl->pass, k.h_buffer, reinterpret_cast<dg_stream_t>(cs)) != 0)
-        rc = DG_ERR_CUDA;
+    // The built-in denoiser feeding an E4M3 head quantises the rows it writes in the same kernel
+    // (the bf16 hidden states are still written to h_buffer).
+    const bool fuse_quant = k.fn == dg_synth_denoise && P.path == PATH_TC_E4M3_QUANT;
+    Prepared Ph = P;
+    if (fuse_quant) {
+        const dg_synth_params& sp = E->synth_user;
+        if (launch_synth_denoise(sp.desc, sp.y, sp.n_content, sp.s_content, sp.s_pad, k.canvas,
+                                 &ctl->pass, static_cast<uint16_t*>(k.h_buffer), sp.status, cs,
+                                 ws + P.L.off_qh, reinterpret_cast<float*>(ws + P.L.off_sch)) !=
+            cudaSuccess)
+            rc = DG_ERR_CUDA;
+        Ph.path = -PATH_TC_E4M3_QUANT;  // quantisation already done
+    } else {
+        void* user = (k.fn == dg_synth_denoise) ? static_cast<void*>(&E->synth_user) : k.user;
+        if (k.fn(user, k.canvas, &ctl->pass, k.h_buffer, reinterpret_cast<dg_stream_t>(cs)) != 0)
+            rc = DG_ERR_CUDA;
+    }
     const size_t hbytes = static_cast<size_t>(d->B) * d->S * d->d * elem_size(d->h_dtype);
     if (rc == DG_OK && k.params.trace_h &&
         launch_trace_copy(k.h_buffer, k.params.trace_h, hbytes, ctl, cs) != cudaSuccess)
         rc = DG_ERR_CUDA;
-    if (rc == DG_OK && enqueue_head(d, P, ws, k.status, cs) != cudaSuccess) rc = DG_ERR_CUDA;
+    if (rc == DG_OK && enqueue_head(d, Ph, ws, k.status, cs) != cudaSuccess) rc = DG_ERR_CUDA;
     if (rc == DG_OK) {
         SelectArgs s = base_select(d, P, ws, k.status);
         set_stats(&s, P, ws, k.argmax, k.conf, k.entropy);
@@ -556,13 +612,20 @@ extern "C" int dg_canvas_loop(const dg_head_desc* desc, int32_t* canvas, void* h
 
     LoopKey key;
     std::memset(&key, 0, sizeof(key));
-    key.desc = *desc;
+    copy_desc(&key.desc, *desc);
     key.canvas = canvas;
     key.h_buffer = h_buffer;
-    key.params = *params;
+    copy_params(&key.params, *params);
     key.fn = denoise;
     key.user = user;
-    if (denoise == dg_synth_denoise) key.synth = *static_cast<dg_synth_params*>(user);
+    if (denoise == dg_synth_denoise) {
+        // compare the built-in denoiser's parameters by value, not by the caller's (often
+        // short-lived) host structs, so repeated calls reuse the captured graph
+        key.user = nullptr;
+        copy_synth(&key.synth, *static_cast<dg_synth_params*>(user));
+        copy_desc(&key.synth_desc, *key.synth.desc);
+        key.synth.desc = nullptr;
+    }
     key.state = state;
     key.argmax = argmax;
     key.conf = conf;
@@ -584,7 +647,7 @@ extern "C" int dg_canvas_loop(const dg_head_desc* desc, int32_t* canvas, void* h
         E = new LoopEntry();
         E->key = key;
         if (denoise == dg_synth_denoise) {
-            E->synth_desc = *key.synth.desc;
+            E->synth_desc = key.synth_desc;
             E->synth_user = key.synth;
             E->synth_user.desc = &E->synth_desc;
         }

@@ -22,7 +22,7 @@ __global__ void __launch_bounds__(BM)
     __shared__ __align__(16) float ws[BN][KC];
     const int t = threadIdx.x;
     const int units = args.MB * args.n_groups;
-    zero_tickets(args);
+    grid_dependency_wait();
     grid_launch_dependents();
     for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
         const int mb = unit % args.MB, grp = unit / args.MB;
@@ -85,8 +85,15 @@ __global__ void __launch_bounds__(BM)
 
 cudaError_t launch_head_simt(const float* h, const float* w, const HeadArgs& args, int grid,
                              cudaStream_t stream) {
-    head_simt_kernel<<<grid, BM, 0, stream>>>(h, w, args);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(BM);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    set_pdl_attr(&attr[0]);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, head_simt_kernel, h, w, args);
 }
 
 }  // namespace dg

@@ -69,8 +69,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int units = args.MB * args.n_groups;
-    zero_tickets(args);
-    grid_launch_dependents();
     constexpr int KB_ELEMS = (KIND == 0) ? 64 : 128;  // elements per 128-byte K slice
 
     if (threadIdx.x == 0) {
@@ -96,6 +94,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
+    grid_dependency_wait();  // the prologue above overlaps the previous kernel of the stream
+    grid_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -270,25 +270,26 @@ cudaError_t launch_head_tc(int kind, const void* h, const void* w, const HeadArg
         return cudaErrorInvalidValue;
     if (plan.pair) return launch_head_tc2(kind, ma, mb, args, plan.grid, stream);
     static bool attr_set[2] = {false, false};
-    if (kind == 0) {
-        if (!attr_set[0]) {
-            cudaError_t e = cudaFuncSetAttribute(head_tc_kernel<0>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 SMEM_BYTES);
-            if (e != cudaSuccess) return e;
-            attr_set[0] = true;
-        }
-        head_tc_kernel<0><<<plan.grid, kTcThreads, SMEM_BYTES, stream>>>(ma, mb, args);
-    } else {
-        if (!attr_set[1]) {
-            cudaError_t e = cudaFuncSetAttribute(head_tc_kernel<1>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 SMEM_BYTES);
-            if (e != cudaSuccess) return e;
-            attr_set[1] = true;
-        }
-        head_tc_kernel<1><<<plan.grid, kTcThreads, SMEM_BYTES, stream>>>(ma, mb, args);
+    const void* fn = kind == 0 ? reinterpret_cast<const void*>(head_tc_kernel<0>)
+                               : reinterpret_cast<const void*>(head_tc_kernel<1>);
+    if (!attr_set[kind]) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set[kind] = true;
     }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    set_pdl_attr(&attr[0]);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = kind == 0 ? cudaLaunchKernelEx(&cfg, head_tc_kernel<0>, ma, mb, args)
+                              : cudaLaunchKernelEx(&cfg, head_tc_kernel<1>, ma, mb, args);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

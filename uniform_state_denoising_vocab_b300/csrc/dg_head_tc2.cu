@@ -83,8 +83,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int pair = blockIdx.x >> 1;
     const int n_pairs = gridDim.x >> 1;
     const int units = args.MB * args.n_groups;  // MB counts 256-row blocks here
-    zero_tickets(args);
-    grid_launch_dependents();
     constexpr int KB_ELEMS = (KIND == 0) ? 64 : 128;
 
     if (threadIdx.x == 0) {
@@ -110,6 +108,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     cluster_sync();  // barriers of both CTAs initialised and TMEM allocated before any use
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
+    grid_dependency_wait();  // the prologue above overlaps the previous kernel of the stream
+    grid_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -263,13 +263,14 @@ cudaError_t launch_head_tc2(int kind, const CUtensorMap& ma, const CUtensorMap& 
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    set_pdl_attr(&attr[1]);
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (kind == 0) return cudaLaunchKernelEx(&cfg, head_tc2_kernel<0>, ma, mb, args);
     return cudaLaunchKernelEx(&cfg, head_tc2_kernel<1>, ma, mb, args);
 }

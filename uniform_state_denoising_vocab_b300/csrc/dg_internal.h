@@ -22,7 +22,7 @@ constexpr int kSimtBN = 64;
 
 // Work decomposition of a head pass: MB row blocks x NT vocabulary tiles, each row block split
 // into n_groups vocabulary groups (group g takes tiles g, g + n_groups, ...). A (row block,
-// group) unit writes one Partial per row into partials[g * R + row].
+// group) unit writes one Partial per row into partials[row * n_groups + g].
 // For the CTA-pair kernel (pair = 1) a row block is 256 rows and `grid` counts pairs.
 struct HeadPlan {
     int R, V, d;
@@ -42,22 +42,23 @@ struct HeadArgs {
     const float* h_scale;     // [R] or null
     const float* w_scale;     // [V] or null
     float4* partials;         // [R][n_groups]: the partials of one row are contiguous
-    uint32_t* tickets;        // [n_tickets] per-canvas arrival counters of the merge, zeroed here
-    int n_tickets;
     uint32_t* status;         // sticky status word or null
 };
 
-// The merge kernel's per-canvas arrival counters start every pass at zero: each head launch
-// (which precedes the merge in stream order) clears them.
-__device__ __forceinline__ void zero_tickets(const HeadArgs& a) {
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.n_tickets; i += gridDim.x * blockDim.x)
-        a.tickets[i] = 0;
+// Programmatic dependent launch. Every kernel of a pass is launched with the programmatic
+// stream-serialization attribute, so it may be scheduled while its predecessor in the stream is
+// still running; it calls grid_dependency_wait() before its first global-memory access, which
+// returns once the predecessor grid has completed and its writes are visible (a no-op for a
+// normal launch). grid_launch_dependents() lets the successor be scheduled early.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
-
-// Allow the dependent launch (the merge kernel) to be scheduled now; it still waits for this
-// grid's completion before reading anything.
 __device__ __forceinline__ void grid_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+inline void set_pdl_attr(cudaLaunchAttribute* a) {
+    a->id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a->val.programmaticStreamSerializationAllowed = 1;
 }
 
 // Tensor-core head (bf16: kind = 0, e4m3: kind = 1). h and w are device row-major matrices.
@@ -83,7 +84,6 @@ struct LoopCtl {
 struct SelectArgs {
     const float4* partials;           // [R][n_groups]
     int n_groups, R, S, B, V;
-    uint32_t* tickets;                // [B] arrival counters (zero on entry, left zero on exit)
     int32_t* argmax;                  // per-row statistics: caller's arrays or workspace scratch
     float* conf;
     float* entropy;
@@ -126,10 +126,12 @@ cudaError_t launch_loop_init(int32_t* canvas, int R, int S, int B, int V, uint64
 cudaError_t launch_trace_copy(const void* src, void* dst, size_t bytes, const LoopCtl* ctl,
                               cudaStream_t stream);
 
-// Built-in synthetic denoiser.
+// Built-in synthetic denoiser. With q_out/scale_out non-null it also quantises each bf16 row
+// it writes to E4M3 with the per-row absmax rule of launch_quant_rows (one kernel instead of two).
 cudaError_t launch_synth_denoise(const dg_head_desc* desc, const int32_t* y, int n_content,
                                  float s_content, float s_pad, const int32_t* canvas,
                                  const int32_t* pass, uint16_t* h_out, uint32_t* status,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, uint8_t* q_out = nullptr,
+                                 float* scale_out = nullptr);
 
 }  // namespace dg

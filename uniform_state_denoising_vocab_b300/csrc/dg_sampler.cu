@@ -21,6 +21,7 @@
 
 #include "dg_common.cuh"
 #include "dg_internal.h"
+#include "dg_ptx.cuh"
 
 namespace dg {
 namespace {
@@ -34,201 +35,268 @@ __device__ __forceinline__ Partial shfl_xor_partial(const Partial& p, int off) {
     return q;
 }
 
-// Wait until the grid this launch depends on (the head kernel, when launched as a programmatic
-// dependent) has completed and its memory is visible. A no-op for a normal launch.
-__device__ __forceinline__ void grid_dependency_wait() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+// ---------------------------------------------------------------------------------------------
+// The per-canvas step, on one thread-block cluster per canvas (kMergeCluster CTAs).
+// ---------------------------------------------------------------------------------------------
+constexpr int kMergeCluster = 8;              // CTAs per canvas (one cluster)
+constexpr int kMergeThreads = 1024;           // 32 warps per CTA: one slot row per warp at S = 256
+constexpr int kMergeWarps = kMergeThreads / 32;
+constexpr int kMaxRowsPerCta = 1024 / kMergeCluster;
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
-constexpr int kMergeWarps = 16;            // slot rows merged per CTA (one warp per row)
-constexpr int kMergeThreads = kMergeWarps * 32;
+struct MergeSmem {
+    float conf[kMaxRowsPerCta];      // this CTA's rows: confidence, entropy, argmax
+    float ent[kMaxRowsPerCta];
+    int32_t arg[kMaxRowsPerCta];
+    int32_t old[kMaxRowsPerCta];     // this CTA's slots' tokens before the pass
+    float all_conf[1024];            // every slot of the canvas (gathered over the cluster)
+    float warp_ent[32];              // CTA 0: per-warp sums of the entropy tree
+    uint32_t changed[kMergeCluster]; // CTA 0: per-CTA "some slot changed" flags (pushed)
+};
 
-// Per-canvas part of a pass, run by the last CTA of the canvas to finish its rows:
-// mean entropy (fixed-order pairwise tree over the slots), rank by (confidence desc, slot asc),
-// keep the top K at their argmax, re-draw the rest with the counter key, stop rules.
-__device__ void canvas_tail(const SelectArgs& a, int b, int p, bool frozen, float* sh_red,
-                            float* sh_conf, int rows_pow2) {
-    const int tid = threadIdx.x;
-    const int base = b * a.S;
+// Cluster b (kMergeCluster CTAs of kMergeThreads) handles canvas b. CTA c owns slots
+// [c * rpc, (c + 1) * rpc) with rpc = ceil(S / kMergeCluster); warp w merges the vocabulary-group
+// partials of its slots w, w + 16, ...: lane l takes groups l, l + 32, ... in increasing order,
+// then the lanes combine with a fixed xor butterfly (lower lane first), so every run merges in
+// the same order and all lanes end with the same result. After a cluster barrier every CTA reads
+// the whole canvas's confidences from the cluster's shared memory and ranks its own slots by
+// (confidence desc, slot asc): kept <=> rank < K; kept slots take their argmax, the others the
+// counter-hash draw. CTA 0 forms the mean entropy (fixed-order pairwise tree over the slots) and,
+// after a second barrier, applies the stop rules; in loop mode the last canvas of the pass
+// advances the pass and sets the graph condition.
+__global__ void __cluster_dims__(kMergeCluster, 1, 1) __maxnreg__(40)
+    merge_select_kernel(const SelectArgs a) {
+    __shared__ MergeSmem sm;
+    grid_dependency_wait();
+    const int b = blockIdx.x / kMergeCluster;
+    const uint32_t c = cluster_ctarank();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int S = a.S;
+    const int rpc = (S + kMergeCluster - 1) / kMergeCluster;
+    const int j0 = static_cast<int>(c) * rpc;
+    const int nrows = max(0, min(rpc, S - j0));
+    const int base = b * S;
+    const int p = a.ctl ? a.ctl->pass : static_cast<int>(a.pass);
+    const bool frozen = a.state != nullptr && a.state[b].done != 0;  // same in every CTA of b
+
     if (frozen) {
         if (a.canvas_out && a.canvas_out != a.canvas_in)
-            for (int j = tid; j < a.S; j += blockDim.x) a.canvas_out[base + j] = a.canvas_in[base + j];
-        return;
-    }
-    // statistics of the canvas's rows, written by every CTA of the canvas (L2, not L1)
-    for (int j = tid; j < rows_pow2; j += blockDim.x) {
-        sh_red[j] = j < a.S ? __ldcg(a.entropy + base + j) : 0.0f;
-        sh_conf[j] = j < a.S ? __ldcg(a.conf + base + j) : 0.0f;
-    }
-    __syncthreads();
-    for (int off = rows_pow2 >> 1; off > 0; off >>= 1) {
-        for (int j = tid; j < off; j += blockDim.x) sh_red[j] += sh_red[j + off];
-        __syncthreads();
-    }
-    const float meanH = sh_red[0] / static_cast<float>(a.S);
-    if (tid == 0 && a.mean_entropy) a.mean_entropy[b] = meanH;
-    if (tid == 0 && a.trace_mean_entropy && a.ctl) a.trace_mean_entropy[p * a.B + b] = meanH;
-    if (!a.canvas_out) return;
+            for (int jj = tid; jj < nrows; jj += kMergeThreads)
+                a.canvas_out[base + j0 + jj] = a.canvas_in[base + j0 + jj];
+    } else {
+        // the old tokens of this CTA's slots, fetched while the partials are merged
+        int old_tok = 0;
+        if (a.canvas_out && tid < nrows) old_tok = a.canvas_in[base + j0 + tid];
 
-    long long K;
-    if (a.keep_sched)
-        K = a.keep_sched[p];
-    else if (a.keep_k0 >= 0)
-        K = static_cast<long long>(a.keep_k0) * (p + 1);
-    else
-        K = a.keep_k;
-    K = K < 0 ? 0 : (K > a.S ? a.S : K);
-
-    // tpr threads per slot (a power of two dividing 32) split the rank count
-    int tpr = static_cast<int>(blockDim.x) / rows_pow2;
-    tpr = tpr < 1 ? 1 : (tpr > 8 ? 8 : tpr);
-    const int sub = tid % tpr;
-    const int slots_per_round = static_cast<int>(blockDim.x) / tpr;
-    int changed = 0;
-    for (int j0 = 0; j0 < rows_pow2; j0 += slots_per_round) {
-        const int j = j0 + tid / tpr;
-        const bool act = j < a.S;
-        const float cj = act ? sh_conf[j] : 0.0f;
-        int rank = 0;
-        if (act)
-            for (int i = sub; i < a.S; i += tpr) {
-                const float ci = sh_conf[i];
-                rank += (ci > cj) || (ci == cj && i < j);
+        for (int jj = warp; jj < nrows; jj += kMergeWarps) {
+            const int r = base + j0 + jj;
+            const float4* q = a.partials + static_cast<size_t>(r) * a.n_groups;
+            Partial acc = partial_empty();
+            // all of this lane's partials (groups lane, lane + 32, ...) in flight at once,
+            // then merged in increasing group order
+            for (int g0 = 0; g0 < a.n_groups; g0 += 4 * 32) {
+                float4 v[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int g = g0 + lane + 32 * i;
+                    v[i] = g < a.n_groups ? __ldcg(q + g) : pack(partial_empty());
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc = partial_merge(acc, unpack(v[i]));
             }
-        for (int off = 1; off < tpr; off <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, off);
-        if (act && sub == 0) {
-            const int r = base + j;
-            const bool kp = rank < K;
-            const int old = a.canvas_in[r];
-            const int nw = kp ? __ldcg(a.argmax + r)
-                              : static_cast<int>(draw_key(a.seed, static_cast<uint32_t>(p),
-                                                          static_cast<uint64_t>(r)) %
-                                                 static_cast<uint64_t>(a.V));
-            if (old < 0 || old >= a.V) flag_status(a.status, DG_ST_BAD_TOKEN);
-            if (a.trace_canvas && a.ctl) a.trace_canvas[static_cast<size_t>(p) * a.R + r] = old;
-            a.canvas_out[r] = nw;
-            if (a.kept) a.kept[r] = kp ? 1 : 0;
-            changed |= (nw != old);
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const Partial o = shfl_xor_partial(acc, off);
+                acc = (lane & off) ? partial_merge(o, acc) : partial_merge(acc, o);
+            }
+            if (lane == 0) {
+                const float s = acc.s;
+                const float conf = 1.0f / s;
+                const float H = fmaxf(kLn2 * (log2f(s) - acc.u / s), 0.0f);
+                if (!(isfinite(s) && isfinite(acc.u) && isfinite(acc.mx) && s >= 1.0f - 1e-3f))
+                    flag_status(a.status, DG_ST_NONFINITE);
+                sm.conf[jj] = conf;
+                sm.ent[jj] = H;
+                sm.arg[jj] = acc.idx;
+                a.argmax[r] = acc.idx;
+                a.conf[r] = conf;
+                a.entropy[r] = H;
+                if (a.ctl) {
+                    const size_t tr = static_cast<size_t>(p) * a.R + r;
+                    if (a.trace_argmax) a.trace_argmax[tr] = acc.idx;
+                    if (a.trace_conf) a.trace_conf[tr] = conf;
+                    if (a.trace_entropy) a.trace_entropy[tr] = H;
+                }
+            }
+        }
+        if (tid < nrows) sm.old[tid] = old_tok;
+        cluster_sync();  // every CTA's statistics are in its shared memory
+
+        // gather the canvas's confidences from the cluster; CTA 0 also sums the entropies with a
+        // fixed-order tree: pairwise within each warp of 32 consecutive slots (xor butterfly),
+        // then the per-warp sums in increasing order
+        float ent_i = 0.0f;
+        for (int i = tid; i < S; i += kMergeThreads) {
+            const uint32_t owner = static_cast<uint32_t>(i / rpc);
+            const int off = i - static_cast<int>(owner) * rpc;
+            sm.all_conf[i] = ld_cluster_f32(mapa_shared(smem_u32(&sm.conf[off]), owner));
+            if (c == 0) ent_i = ld_cluster_f32(mapa_shared(smem_u32(&sm.ent[off]), owner));
+        }
+        if (c == 0) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ent_i += __shfl_xor_sync(0xffffffffu, ent_i, off);
+            if (lane == 0) sm.warp_ent[warp] = ent_i;
+        }
+        __syncthreads();
+
+        uint32_t changed = 0;
+        if (a.canvas_out) {
+            long long K;
+            if (a.keep_sched)
+                K = a.keep_sched[p];
+            else if (a.keep_k0 >= 0)
+                K = static_cast<long long>(a.keep_k0) * (p + 1);
+            else
+                K = a.keep_k;
+            K = K < 0 ? 0 : (K > S ? S : K);
+            // tpr threads per slot (a power of two dividing 32) split the rank count
+            const int rpow2 = max(1, 1 << (32 - __clz(max(nrows, 1) - 1)));
+            int tpr = kMergeThreads / rpow2;
+            tpr = tpr > 32 ? 32 : tpr;
+            const int jj = tid / tpr, sub = tid % tpr;
+            int rank = 0;
+            const bool act = jj < nrows;
+            const int j = j0 + jj;
+            if (act) {
+                const float cj = sm.all_conf[j];
+                for (int i = sub; i < S; i += tpr) {
+                    const float ci = sm.all_conf[i];
+                    rank += (ci > cj) || (ci == cj && i < j);
+                }
+            }
+            for (int off = 1; off < tpr; off <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, off);
+            if (act && sub == 0) {
+                const int r = base + j;
+                const bool kp = rank < K;
+                const int oldt = sm.old[jj];
+                const int nw = kp ? sm.arg[jj]
+                                  : static_cast<int>(draw_key(a.seed, static_cast<uint32_t>(p),
+                                                              static_cast<uint64_t>(r)) %
+                                                     static_cast<uint64_t>(a.V));
+                if (oldt < 0 || oldt >= a.V) flag_status(a.status, DG_ST_BAD_TOKEN);
+                if (a.trace_canvas && a.ctl) a.trace_canvas[static_cast<size_t>(p) * a.R + r] = oldt;
+                a.canvas_out[r] = nw;
+                if (a.kept) a.kept[r] = kp ? 1 : 0;
+                changed = (nw != oldt);
+            }
+        }
+        changed = __syncthreads_or(changed);
+        if (tid == 0) st_cluster_u32(mapa_shared(smem_u32(&sm.changed[c]), 0), changed);
+
+        float meanH = 0.0f;
+        if (c == 0) {
+            const int nw = (S + 31) / 32;
+            float sum = 0.0f;
+            for (int i = 0; i < nw; ++i) sum += sm.warp_ent[i];
+            meanH = sum / static_cast<float>(S);
+        }
+        cluster_sync();  // changed flags delivered; no CTA reads another's shared memory after this
+        if (c != 0) return;
+        if (tid == 0) {
+            if (a.mean_entropy) a.mean_entropy[b] = meanH;
+            if (a.trace_mean_entropy && a.ctl) a.trace_mean_entropy[p * a.B + b] = meanH;
+            if (a.canvas_out && a.state && a.has_rule) {
+                uint32_t any = 0;
+                for (int i = 0; i < kMergeCluster; ++i) any |= sm.changed[i];
+                dg_canvas_state st = a.state[b];
+                st.stable = any ? 0 : st.stable + 1;
+                const bool ent = meanH < a.rule.entropy_threshold;
+                const bool stb = st.stable >= a.rule.stable_passes;
+                const bool cap = p + 1 >= a.rule.max_passes;
+                const bool stop =
+                    (a.rule.stop_mode == DG_STOP_AND ? (ent && stb) : (ent || stb)) || cap;
+                st.mean_entropy = meanH;
+                st.last_pass = p;
+                if (stop) {
+                    st.done = 1;
+                    st.passes = p + 1;
+                    st.reason = (ent ? DG_REASON_ENTROPY : 0) | (stb ? DG_REASON_STABLE : 0) |
+                                (cap ? DG_REASON_CAP : 0);
+                }
+                a.state[b] = st;
+            }
         }
     }
-    changed = __syncthreads_or(changed);
-    if (tid == 0 && a.state && a.has_rule) {
-        dg_canvas_state st = a.state[b];
-        st.stable = changed ? 0 : st.stable + 1;
-        const bool ent = meanH < a.rule.entropy_threshold;
-        const bool stb = st.stable >= a.rule.stable_passes;
-        const bool cap = p + 1 >= a.rule.max_passes;
-        const bool stop = (a.rule.stop_mode == DG_STOP_AND ? (ent && stb) : (ent || stb)) || cap;
-        st.mean_entropy = meanH;
-        st.last_pass = p;
-        if (stop) {
-            st.done = 1;
-            st.passes = p + 1;
-            st.reason = (ent ? DG_REASON_ENTROPY : 0) | (stb ? DG_REASON_STABLE : 0) |
-                        (cap ? DG_REASON_CAP : 0);
+
+    // loop mode: the last canvas of the pass advances the pass and sets the graph condition
+    if (a.ctl && c == 0 && tid == 0) {
+        unsigned t = 0;
+        if (a.B > 1) {
+            __threadfence();
+            t = atomicAdd(&a.ctl->ticket, 1u);
         }
-        a.state[b] = st;
+        if (t == static_cast<unsigned>(a.B) - 1u) {
+            if (a.B > 1) __threadfence();
+            int all_done = 1;
+            if (a.state)
+                for (int bb = 0; bb < a.B; ++bb)
+                    all_done &= (*reinterpret_cast<volatile int*>(&a.state[bb].done) != 0);
+            else
+                all_done = 0;
+            a.ctl->ticket = 0;
+            const int np = p + 1;
+            a.ctl->pass = np;
+            if (a.set_cond)
+                cudaGraphSetConditional(a.cond, (!all_done && np < a.ctl->max_passes) ? 1u : 0u);
+        }
     }
 }
 
-// Grid: B x ceil(S / kMergeWarps) CTAs of kMergeThreads. Warp w of CTA (b, x) merges the
-// vocabulary-group partials of slot x * kMergeWarps + w of canvas b: lane l takes groups
-// l, l + 32, ... in increasing order, then the lanes combine with a fixed xor butterfly (lower
-// lane first), so every run merges in the same order and all lanes end with the same result.
-// The last CTA of a canvas to arrive (arrival counter in a.tickets) runs the canvas tail; in
-// loop mode the last canvas tail of the pass advances the pass and sets the graph condition.
-__global__ void __launch_bounds__(kMergeThreads) merge_select_kernel(const SelectArgs a,
-                                                                      int ctas_per_canvas) {
-    extern __shared__ float sh[];  // [2 * rows_pow2]: entropy tree, confidences
-    __shared__ int sh_last;
-    grid_dependency_wait();
-    const int rows_pow2 = max(32, 1 << (32 - __clz(a.S - 1)));
-    const int b = blockIdx.x / ctas_per_canvas;
-    const int x = blockIdx.x % ctas_per_canvas;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int j = x * kMergeWarps + warp;
-    const int p = a.ctl ? a.ctl->pass : static_cast<int>(a.pass);
-    const bool frozen = a.state != nullptr && a.state[b].done != 0;
-
-    if (!frozen && j < a.S) {
-        const int r = b * a.S + j;
-        const float4* q = a.partials + static_cast<size_t>(r) * a.n_groups;
-        Partial acc = partial_empty();
-        int g = lane;
-        for (; g + 96 < a.n_groups; g += 128) {
-            const float4 v0 = __ldcg(q + g), v1 = __ldcg(q + g + 32), v2 = __ldcg(q + g + 64),
-                         v3 = __ldcg(q + g + 96);
-            acc = partial_merge(acc, unpack(v0));
-            acc = partial_merge(acc, unpack(v1));
-            acc = partial_merge(acc, unpack(v2));
-            acc = partial_merge(acc, unpack(v3));
-        }
-        for (; g < a.n_groups; g += 32) acc = partial_merge(acc, unpack(__ldcg(q + g)));
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const Partial o = shfl_xor_partial(acc, off);
-            acc = (lane & off) ? partial_merge(o, acc) : partial_merge(acc, o);
-        }
-        if (lane == 0) {
-            const float s = acc.s;
-            const float conf = 1.0f / s;
-            const float H = fmaxf(kLn2 * (log2f(s) - acc.u / s), 0.0f);
-            if (!(isfinite(s) && isfinite(acc.u) && isfinite(acc.mx) && s >= 1.0f - 1e-3f))
-                flag_status(a.status, DG_ST_NONFINITE);
-            a.argmax[r] = acc.idx;
-            a.conf[r] = conf;
-            a.entropy[r] = H;
-            if (a.ctl) {
-                const size_t tr = static_cast<size_t>(p) * a.R + r;
-                if (a.trace_argmax) a.trace_argmax[tr] = acc.idx;
-                if (a.trace_conf) a.trace_conf[tr] = conf;
-                if (a.trace_entropy) a.trace_entropy[tr] = H;
-            }
-        }
-    }
-
-    // arrival: the last CTA of canvas b (in arrival order) sees every row's statistics
+// Block-wide max of a non-negative value (blockDim.x a multiple of 32, at most 1024).
+__device__ __forceinline__ float block_max(float v, float* red) {
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    __syncthreads();  // `red` may still be in use by a previous reduction
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned t = atomicAdd(&a.tickets[b], 1u);
-        sh_last = (t == static_cast<unsigned>(ctas_per_canvas) - 1u);
-        if (sh_last) {
-            a.tickets[b] = 0;  // ready for the next pass
-            __threadfence();
-        }
+    if (threadIdx.x < 32) {
+        float m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (threadIdx.x == 0) red[0] = m;
     }
     __syncthreads();
-    if (!sh_last) return;
-    canvas_tail(a, b, p, frozen, sh, sh + rows_pow2, rows_pow2);
+    return red[0];
+}
 
-    // loop mode: the last canvas tail of the pass advances the pass and sets the graph condition
-    if (a.ctl) {
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            __threadfence();
-            const unsigned t = atomicAdd(&a.ctl->ticket, 1u);
-            if (t == static_cast<unsigned>(a.B) - 1u) {
-                __threadfence();
-                int all_done = 1;
-                if (a.state)
-                    for (int bb = 0; bb < a.B; ++bb)
-                        all_done &= (*reinterpret_cast<volatile int*>(&a.state[bb].done) != 0);
-                else
-                    all_done = 0;
-                a.ctl->ticket = 0;
-                const int np = p + 1;
-                a.ctl->pass = np;
-                if (a.set_cond)
-                    cudaGraphSetConditional(a.cond, (!all_done && np < a.ctl->max_passes) ? 1u : 0u);
-            }
-        }
+// E4M3 codes of one bf16 row given its absmax: amax = 0 gives scale 1 and all-zero codes,
+// otherwise inv = fp32(448 / amax), q_k = e4m3_rn_satfinite(fp32(h_k * inv)), scale = amax / 448.
+__device__ __forceinline__ void quant_row(const __nv_bfloat16* hr, int d, float amax, uint8_t* qr,
+                                          float* scale) {
+    if (amax == 0.f) {
+        for (int k = threadIdx.x; k < d; k += blockDim.x) qr[k] = 0;
+        if (threadIdx.x == 0) *scale = 1.0f;
+        return;
     }
+    const float inv = __fdiv_rn(448.0f, amax);
+    for (int k = threadIdx.x; k < d; k += blockDim.x) {
+        const float x = __fmul_rn(__bfloat162float(hr[k]), inv);
+        qr[k] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
+    }
+    if (threadIdx.x == 0) *scale = __fdiv_rn(amax, 448.0f);
 }
 
 __global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ h, int d, uint8_t* __restrict__ q,
                                   float* __restrict__ scale, uint32_t* status) {
     __shared__ float red[32];
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int r = blockIdx.x;
     const __nv_bfloat16* hr = h + static_cast<size_t>(r) * d;
     float amax = 0.f;
@@ -239,28 +307,8 @@ __global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ h, int d, ui
         amax = fmaxf(amax, fabsf(v));
     }
     if (__syncthreads_or(bad) && threadIdx.x == 0) flag_status(status, DG_ST_NONFINITE);
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        float m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (threadIdx.x == 0) red[0] = m;
-    }
-    __syncthreads();
-    amax = red[0];
-    uint8_t* qr = q + static_cast<size_t>(r) * d;
-    if (amax == 0.f) {
-        for (int k = threadIdx.x; k < d; k += blockDim.x) qr[k] = 0;
-        if (threadIdx.x == 0) scale[r] = 1.0f;
-        return;
-    }
-    const float inv = __fdiv_rn(448.0f, amax);
-    for (int k = threadIdx.x; k < d; k += blockDim.x) {
-        const float x = __fmul_rn(__bfloat162float(hr[k]), inv);
-        qr[k] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
-    }
-    if (threadIdx.x == 0) scale[r] = __fdiv_rn(amax, 448.0f);
+    amax = block_max(amax, red);
+    quant_row(hr, d, amax, q + static_cast<size_t>(r) * d, scale + r);
 }
 
 __global__ void loop_init_kernel(int32_t* canvas, int S, int V, uint64_t seed, int init_random,
@@ -324,8 +372,11 @@ __global__ void synth_denoise_kernel(int dtype, const void* __restrict__ w, cons
                                      int d, int V, const int32_t* __restrict__ y, int n_content,
                                      float s_content, float s_pad, const int32_t* __restrict__ canvas,
                                      const int32_t* __restrict__ pass, __nv_bfloat16* __restrict__ h,
-                                     uint32_t* status) {
+                                     uint32_t* status, uint8_t* __restrict__ q,
+                                     float* __restrict__ qscale) {
     __shared__ float red[32];
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int r = blockIdx.x;
     const int t = pass[0] + 1;
     const float at = fminf(1.0f, __fdiv_rn(static_cast<float>(2 + t), 10.0f));
@@ -335,6 +386,10 @@ __global__ void synth_denoise_kernel(int dtype, const void* __restrict__ w, cons
     if (yy < 0 || yy >= V || cc < 0 || cc >= V) {
         if (threadIdx.x == 0) flag_status(status, DG_ST_BAD_TOKEN);
         for (int k = threadIdx.x; k < d; k += blockDim.x) hr[k] = __float2bfloat16_rn(0.f);
+        if (q) {
+            for (int k = threadIdx.x; k < d; k += blockDim.x) q[static_cast<size_t>(r) * d + k] = 0;
+            if (threadIdx.x == 0) qscale[r] = 1.0f;
+        }
         return;
     }
     float n2 = 0.f;
@@ -354,43 +409,214 @@ __global__ void synth_denoise_kernel(int dtype, const void* __restrict__ w, cons
     n2 = red[0];
     const float s = (r % S) < n_content ? s_content : s_pad;
     const float inv = n2 > 0.f ? s / sqrtf(n2) : 0.f;
+    float amax = 0.f;
+    bool bad = false;
     for (int k = threadIdx.x; k < d; k += blockDim.x) {
         const float x = at * head_value(dtype, w, ws, yy, d, k) + bt * head_value(dtype, w, ws, cc, d, k);
-        hr[k] = __float2bfloat16_rn(x * inv);
+        const __nv_bfloat16 hb = __float2bfloat16_rn(x * inv);
+        hr[k] = hb;
+        const float v = __bfloat162float(hb);
+        bad |= !isfinite(v);
+        amax = fmaxf(amax, fabsf(v));
+    }
+    if (q) {
+        if (__syncthreads_or(bad) && threadIdx.x == 0) flag_status(status, DG_ST_NONFINITE);
+        // the row's own bf16 values, written above by this CTA, are visible after the barrier
+        // inside block_max
+        amax = block_max(amax, red);
+        quant_row(hr, d, amax, q + static_cast<size_t>(r) * d, qscale + r);
     }
 }
 
-int pow2_at_least(int x) {
-    int p = 32;
-    while (p < x) p <<= 1;
-    return p;
+// Vectorised synthetic denoiser (same arithmetic as synth_denoise_kernel): one CTA of
+// kDenThreads per row; thread t holds 16-byte chunks t, t + kDenThreads, ... of both head rows
+// (ES-byte elements: 2 = bf16, 1 = E4M3 codes), so the mixed row x stays in registers between the
+// norm, the bf16 write and the optional E4M3 quantisation.
+constexpr int kDenThreads = 128;
+
+template <int ES>
+__device__ __forceinline__ void unpack16(const uint4& v, float scale, float (&out)[16 / ES]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if constexpr (ES == 2) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            out[2 * i] = __uint_as_float(w[i] << 16);
+            out[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
+                static_cast<__nv_fp8x2_storage_t>(w[i] & 0xFFFFu), __NV_E4M3);
+            const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
+                static_cast<__nv_fp8x2_storage_t>(w[i] >> 16), __NV_E4M3);
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+            const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+            out[4 * i] = a.x * scale;
+            out[4 * i + 1] = a.y * scale;
+            out[4 * i + 2] = b.x * scale;
+            out[4 * i + 3] = b.y * scale;
+        }
+    }
+}
+
+__device__ __forceinline__ float block_sum128(float v, float* red) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    return (red[0] + red[1]) + (red[2] + red[3]);
+}
+
+__device__ __forceinline__ float block_max128(float v, float* red) {
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if ((threadIdx.x & 31) == 0) red[4 + (threadIdx.x >> 5)] = v;
+    __syncthreads();
+    return fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7]));
+}
+
+template <int ES, int MAXC>
+__global__ void __launch_bounds__(kDenThreads)
+    synth_denoise_vec_kernel(const uint8_t* __restrict__ w, const float* __restrict__ ws, int S,
+                             int d, int V, const int32_t* __restrict__ y, int n_content,
+                             float s_content, float s_pad, const int32_t* __restrict__ canvas,
+                             const int32_t* __restrict__ pass, __nv_bfloat16* __restrict__ h,
+                             uint32_t* status, uint8_t* __restrict__ q, float* __restrict__ qscale) {
+    constexpr int EPC = 16 / ES;  // elements per 16-byte chunk
+    __shared__ float red[8];
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int r = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int t = pass[0] + 1;
+    const int yy = y[r], cc = canvas[r];
+    const float at = fminf(1.0f, __fdiv_rn(static_cast<float>(2 + t), 10.0f));
+    const float bt = 1.0f - at;
+    __nv_bfloat16* hr = h + static_cast<size_t>(r) * d;
+    const int nch = d / EPC;
+    if (yy < 0 || yy >= V || cc < 0 || cc >= V) {
+        if (tid == 0) flag_status(status, DG_ST_BAD_TOKEN);
+        for (int k = tid; k < d; k += kDenThreads) hr[k] = __float2bfloat16_rn(0.f);
+        if (q) {
+            for (int k = tid; k < d; k += kDenThreads) q[static_cast<size_t>(r) * d + k] = 0;
+            if (tid == 0) qscale[r] = 1.0f;
+        }
+        return;
+    }
+    const uint4* wy = reinterpret_cast<const uint4*>(w + static_cast<size_t>(yy) * d * ES);
+    const uint4* wc = reinterpret_cast<const uint4*>(w + static_cast<size_t>(cc) * d * ES);
+    uint4 vy[MAXC], vc[MAXC];
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+        const int ch = tid + i * kDenThreads;
+        if (ch < nch) {
+            vy[i] = __ldg(wy + ch);
+            vc[i] = __ldg(wc + ch);
+        }
+    }
+    const float sy = ES == 1 ? ws[yy] : 1.0f, sc = ES == 1 ? ws[cc] : 1.0f;
+    float x[MAXC][EPC];
+    float n2 = 0.f;
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+        const int ch = tid + i * kDenThreads;
+        if (ch < nch) {
+            float a[EPC], b[EPC];
+            unpack16<ES>(vy[i], sy, a);
+            unpack16<ES>(vc[i], sc, b);
+#pragma unroll
+            for (int e = 0; e < EPC; ++e) {
+                x[i][e] = at * a[e] + bt * b[e];
+                n2 = fmaf(x[i][e], x[i][e], n2);
+            }
+        }
+    }
+    n2 = block_sum128(n2, red);
+    const float s = (r % S) < n_content ? s_content : s_pad;
+    const float inv = n2 > 0.f ? s / sqrtf(n2) : 0.f;
+    float amax = 0.f;
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+        const int ch = tid + i * kDenThreads;
+        if (ch < nch) {
+            uint32_t packed[EPC / 2];
+#pragma unroll
+            for (int e = 0; e < EPC; e += 2) {
+                const __nv_bfloat16 h0 = __float2bfloat16_rn(x[i][e] * inv);
+                const __nv_bfloat16 h1 = __float2bfloat16_rn(x[i][e + 1] * inv);
+                x[i][e] = __bfloat162float(h0);  // keep the rounded value for the quantiser
+                x[i][e + 1] = __bfloat162float(h1);
+                bad |= !isfinite(x[i][e]) || !isfinite(x[i][e + 1]);
+                amax = fmaxf(amax, fmaxf(fabsf(x[i][e]), fabsf(x[i][e + 1])));
+                packed[e / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
+                                (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(hr + static_cast<size_t>(ch) * EPC);
+#pragma unroll
+            for (int v = 0; v < EPC / 8; ++v)
+                dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+        }
+    }
+    if (!q) return;
+    if (__syncthreads_or(bad) && tid == 0) flag_status(status, DG_ST_NONFINITE);
+    amax = block_max128(amax, red);
+    uint8_t* qr = q + static_cast<size_t>(r) * d;
+    const float qinv = amax == 0.f ? 0.f : __fdiv_rn(448.0f, amax);
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+        const int ch = tid + i * kDenThreads;
+        if (ch < nch) {
+            uint32_t codes[EPC / 4];
+#pragma unroll
+            for (int e = 0; e < EPC; e += 4) {
+                uint32_t c4 = 0;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t cu = amax == 0.f ? 0u
+                        : static_cast<uint32_t>(__nv_cvt_float_to_fp8(__fmul_rn(x[i][e + u], qinv),
+                                                                      __NV_SATFINITE, __NV_E4M3));
+                    c4 |= cu << (8 * u);
+                }
+                codes[e / 4] = c4;
+            }
+            if constexpr (EPC == 16) {
+                reinterpret_cast<uint4*>(qr)[ch] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+            } else {
+                reinterpret_cast<uint2*>(qr)[ch] = make_uint2(codes[0], codes[1]);
+            }
+        }
+    }
+    if (tid == 0) qscale[r] = amax == 0.f ? 1.0f : __fdiv_rn(amax, 448.0f);
 }
 
 }  // namespace
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream) {
-    const int rows = pow2_at_least(a.S);  // 32 .. 1024
-    const int cpc = (a.S + kMergeWarps - 1) / kMergeWarps;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(a.B) * cpc));
+    cfg.gridDim = dim3(static_cast<unsigned>(a.B) * kMergeCluster);
     cfg.blockDim = dim3(kMergeThreads);
-    cfg.dynamicSmemBytes = 2 * rows * sizeof(float);
     cfg.stream = stream;
     // Programmatic dependent launch: the merge grid may be scheduled while the head kernel
     // drains; griddepcontrol.wait at its top orders every read after the head's writes.
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    set_pdl_attr(&attr[0]);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, merge_select_kernel, a, cpc);
+    return cudaLaunchKernelEx(&cfg, merge_select_kernel, a);
 }
 
 cudaError_t launch_quant_rows(const uint16_t* h, int R, int d, uint8_t* q, float* scale,
                               uint32_t* status, cudaStream_t stream) {
-    quant_rows_kernel<<<R, 256, 0, stream>>>(reinterpret_cast<const __nv_bfloat16*>(h), d, q, scale,
-                                             status);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(R);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    set_pdl_attr(&attr[0]);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quant_rows_kernel, reinterpret_cast<const __nv_bfloat16*>(h), d,
+                              q, scale, status);
 }
 
 cudaError_t launch_loop_init(int32_t* canvas, int R, int S, int B, int V, uint64_t seed,
@@ -412,13 +638,38 @@ cudaError_t launch_trace_copy(const void* src, void* dst, size_t bytes, const Lo
 cudaError_t launch_synth_denoise(const dg_head_desc* desc, const int32_t* y, int n_content,
                                  float s_content, float s_pad, const int32_t* canvas,
                                  const int32_t* pass, uint16_t* h_out, uint32_t* status,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, uint8_t* q_out, float* scale_out) {
     const int R = desc->B * desc->S;
-    synth_denoise_kernel<<<R, 256, 0, stream>>>(desc->w_dtype, desc->w, desc->w_scale, desc->S,
-                                                desc->d, desc->V, y, n_content, s_content, s_pad,
-                                                canvas, pass,
-                                                reinterpret_cast<__nv_bfloat16*>(h_out), status);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(R);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    set_pdl_attr(&attr[0]);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    constexpr int MAXC = 4;
+    const int es = desc->w_dtype == DG_BF16 ? 2 : 1;
+    const long long chunks = static_cast<long long>(desc->d) * es / 16;  // d * es % 16 == 0
+    auto hb = reinterpret_cast<__nv_bfloat16*>(h_out);
+    auto wb = static_cast<const uint8_t*>(desc->w);
+    if ((desc->w_dtype == DG_BF16 || desc->w_dtype == DG_E4M3) &&
+        chunks <= static_cast<long long>(MAXC) * kDenThreads) {
+        cfg.blockDim = dim3(kDenThreads);
+        if (es == 2)
+            return cudaLaunchKernelEx(&cfg, synth_denoise_vec_kernel<2, MAXC>, wb, desc->w_scale,
+                                      static_cast<int>(desc->S), static_cast<int>(desc->d),
+                                      static_cast<int>(desc->V), y, n_content, s_content, s_pad,
+                                      canvas, pass, hb, status, q_out, scale_out);
+        return cudaLaunchKernelEx(&cfg, synth_denoise_vec_kernel<1, MAXC>, wb, desc->w_scale,
+                                  static_cast<int>(desc->S), static_cast<int>(desc->d),
+                                  static_cast<int>(desc->V), y, n_content, s_content, s_pad, canvas,
+                                  pass, hb, status, q_out, scale_out);
+    }
+    cfg.blockDim = dim3(256);
+    return cudaLaunchKernelEx(&cfg, synth_denoise_kernel, static_cast<int>(desc->w_dtype),
+                              desc->w, desc->w_scale, static_cast<int>(desc->S),
+                              static_cast<int>(desc->d), static_cast<int>(desc->V), y, n_content,
+                              s_content, s_pad, canvas, pass, hb, status, q_out, scale_out);
 }
 
 }  // namespace dg
