@@ -186,6 +186,29 @@ def roofline(cfg, r, peaks, peak_kind, step_s):
     return out
 
 
+def loop_breakdown(tl, passes):
+    """Mean per-pass durations (us) of the loop's kernels and the gaps between them, from the
+    per-pass kernel timeline: denoise, head, merge, and the gaps denoise->head, head->merge and
+    merge->next pass's denoise (the graph's conditional iteration)."""
+    keys = ("denoise", "gap_denoise_head", "head", "gap_head_merge", "merge", "gap_next_pass")
+    acc = {k: [] for k in keys}
+    for p in range(passes):
+        d, h, m = tl[p]["denoise"], tl[p]["head"], tl[p]["merge"]
+        if d is None or h is None or m is None:
+            continue
+        acc["denoise"].append(d[1] - d[0])
+        acc["gap_denoise_head"].append(h[0] - d[1])
+        acc["head"].append(h[1] - h[0])
+        acc["gap_head_merge"].append(m[0] - h[1])
+        acc["merge"].append(m[1] - m[0])
+        if p + 1 < passes and tl[p + 1]["denoise"] is not None:
+            acc["gap_next_pass"].append(tl[p + 1]["denoise"][0] - m[1])
+    out = {k: (round(statistics.mean(v), 2) if v else None) for k, v in acc.items()}
+    if passes > 1 and tl[0]["denoise"] is not None and tl[passes - 1]["merge"] is not None:
+        out["per_pass"] = round((tl[passes - 1]["merge"][1] - tl[0]["denoise"][0]) / passes, 2)
+    return out
+
+
 def run_ours(args, cfg, ws_, rank):
     import uniform_state_denoising_vocab_b300 as dg
     from workloads import make_loop_inputs, make_pass_inputs
@@ -357,8 +380,14 @@ def run_ours(args, cfg, ws_, rank):
         heads.append(ev)
     torch.cuda.synchronize()
     head_ms = [a.elapsed_time(b) for a, b in heads[len(heads) // 4:]]
+    # in-graph breakdown of one more (untimed) loop from the library's per-pass kernel timeline
+    rt = dg.dg_canvas_loop(w, canvas, timeline=True, **kw)
+    torch.cuda.synchronize()
+    breakdown = loop_breakdown(dg.timeline_us(rt["trace_timeline"], cfg.max_passes),
+                               int(dg.state_fields(rt["state"])["passes"].max()))
     per_pass = 3 + (1 if cfg.precision == "e4m3" else 0)
     return {"t_s": t_ms / 1e3, "units": passes_per_loop * args.steps, "head_ms": head_ms,
+            "loop_breakdown_us": breakdown,
             "clocks": clk.summary(), "status": int(status.item()), "e2e_t_s": e_ms / 1e3,
             "e2e_units": passes_per_loop * e_steps, "h2d": y_host.numel() * 4,
             "d2h": c_back.numel() * 4 + s_back.numel() * 4,
@@ -478,6 +507,7 @@ def main():
         line["roofline"] = roofline(cfg, r, peaks, peak_kind, t_max / args.steps)
         if cfg.mode == "loop":
             line["passes_per_loop"] = r["passes_per_loop"]
+            line["loop_breakdown_us"] = r["loop_breakdown_us"]
             line["roofline"]["step_roof_frac"] = (line["roofline"]["t_roof_us"] * 1e-6 /
                                                   (t_max / r["units"]))
     if not args.no_cpu_baseline and ws_ == 1:

@@ -205,7 +205,16 @@ typedef struct {
     int32_t* trace_argmax;      /* optional device [max_passes * B*S] per-pass statistics */
     float* trace_conf;
     float* trace_entropy;
+    /* optional device [max_passes * DG_TL_KERNELS * 2] uint64: per pass p and kernel k the
+       device global timer (ns) when the first CTA of k got past its wait on the previous kernel
+       (index (p * DG_TL_KERNELS + k) * 2) and when the last CTA of k finished (+1). Entries of
+       passes that did not run, and of the built-in denoiser when the caller supplies its own,
+       stay at (UINT64_MAX, 0). Costs one branch per CTA when NULL. */
+    unsigned long long* trace_timeline;
 } dg_loop_params;
+
+/* Kernels recorded in dg_loop_params.trace_timeline. */
+enum { DG_TL_DENOISE = 0, DG_TL_HEAD = 1, DG_TL_MERGE = 2, DG_TL_KERNELS = 3 };
 
 DG_API int dg_canvas_loop(const dg_head_desc* desc, int32_t* canvas, void* h_buffer,
                    const dg_loop_params* params, dg_denoise_fn denoise, void* user,

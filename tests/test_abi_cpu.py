@@ -52,7 +52,7 @@ int main(void) {
   printf("dg_stop_rule %zu\n", sizeof(dg_stop_rule));
   printf("dg_loop_params %zu\n", sizeof(dg_loop_params));
   P(dg_loop_params, keep_sched) P(dg_loop_params, seed) P(dg_loop_params, start_pass)
-  P(dg_loop_params, trace_h)
+  P(dg_loop_params, trace_h) P(dg_loop_params, trace_entropy) P(dg_loop_params, trace_timeline)
   printf("dg_synth_params %zu\n", sizeof(dg_synth_params));
   P(dg_synth_params, n_content) P(dg_synth_params, s_pad) P(dg_synth_params, status)
   return 0;

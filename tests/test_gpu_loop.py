@@ -264,3 +264,35 @@ def test_denoiser_row_widths(dg, orc, dtype, d):
     assert int(res["status"][0]) == 0
     P, _ = _lockstep(dg, orc, res, cfg, x["w"], x.get("w_scale"), x["y"], dtype)
     assert P >= 1
+
+
+def test_loop_timeline_trace(dg):
+    """The optional per-pass kernel timeline: every pass that ran has ordered denoiser, head and
+    merge intervals (each kernel begins after its predecessor began, and ends after it begins);
+    passes that did not run stay empty; the loop's results are unchanged by tracing."""
+    from workloads import CONFIGS, make_loop_inputs
+    cfg = CONFIGS["loop_bf16_v32768_d256"]
+    x = make_loop_inputs(cfg)
+    tw, ty = dev_bf16(x["w"], (cfg.V, cfg.d)), dev(x["y"])
+    kw = dict(B=cfg.B, S=cfg.S, theta=cfg.theta, y=ty, keep_k0=cfg.keep_k, seed=cfg.seed,
+              max_passes=cfg.max_passes, n_content=cfg.n_content, s_content=cfg.s_content,
+              s_pad=cfg.s_pad)
+    c0 = torch.empty(cfg.R, dtype=torch.int32, device="cuda")
+    r0 = dg.dg_canvas_loop(tw, c0, **kw)
+    c1 = torch.empty(cfg.R, dtype=torch.int32, device="cuda")
+    r1 = dg.dg_canvas_loop(tw, c1, timeline=True, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(c0, c1)
+    P = int(dg.state_fields(r1["state"])["passes"][0])
+    tl = dg.timeline_us(r1["trace_timeline"], cfg.max_passes)
+    prev_end = -1.0
+    for p in range(P):
+        d, h, m = tl[p]["denoise"], tl[p]["head"], tl[p]["merge"]
+        assert d is not None and h is not None and m is not None, p
+        assert d[0] <= d[1] and h[0] <= h[1] and m[0] <= m[1]
+        assert d[0] >= prev_end - 1e-3       # a pass starts after the previous pass ended
+        # each kernel gets past its dependency wait only once its predecessor has finished
+        assert h[0] >= d[1] - 0.1 and m[0] >= h[1] - 0.1
+        prev_end = m[1]
+    for p in range(P, cfg.max_passes):
+        assert tl[p]["head"] is None and tl[p]["merge"] is None

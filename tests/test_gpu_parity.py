@@ -250,3 +250,19 @@ def test_batched_bf16_sampled_rows(dg, orc):
         sl = slice(b * cfg.S, (b + 1) * cfg.S)
         assert g["kept"][sl].sum() == cfg.keep_k
         assert abs(g["mean_entropy"][b] - g["entropy"][sl].astype(np.float64).mean()) < 1e-4
+
+
+@pytest.mark.parametrize("V", [1, 2, 3, 255, 65537, 999983])
+def test_redraw_modulo_edges(dg, orc, V):
+    """With nothing kept every slot is re-drawn: the device's key mod V (computed without the
+    64-bit division routine) equals the oracle's plain modulo for small, prime and odd V."""
+    B, S, d = 2, 256, 16
+    rng = np.random.default_rng(V)
+    h = rng.standard_normal(B * S * d).astype(np.float32)
+    w = (rng.standard_normal(V * d) / 4).astype(np.float32)
+    th, tw = dev_bf16(_bits(h), (B * S, d)), dev_bf16(_bits(w), (V, d))
+    canvas = dev(rng.integers(0, V, B * S).astype(np.int32))
+    for seed, pass_ in ((0, 0), (12345678901234, 47), (2**64 - 1, 0xFFFFFFFE)):
+        r = dg.dg_canvas_step(th, tw, canvas, 0, seed, pass_, B=B, S=S)
+        torch.cuda.synchronize()
+        assert np.array_equal(host(r["canvas"]), orc.draw(seed, pass_, np.arange(B * S), V))

@@ -23,6 +23,7 @@ __all__ = ["DG_F32", "DG_BF16", "DG_E4M3", "HeadDesc", "CanvasState", "StopRule"
            "ST_TIMEOUT", "STOP_OR", "STOP_AND"]
 
 DG_F32, DG_BF16, DG_E4M3 = 0, 1, 2
+DG_TL_DENOISE, DG_TL_HEAD, DG_TL_MERGE, DG_TL_KERNELS = 0, 1, 2, 3
 REASON_ENTROPY, REASON_STABLE, REASON_CAP = 1, 2, 4
 ST_BAD_TOKEN, ST_NONFINITE, ST_TIMEOUT = 1, 2, 4
 STOP_OR, STOP_AND = 0, 1
@@ -60,7 +61,7 @@ class LoopParams(C.Structure):
                 ("seed", C.c_uint64), ("start_pass", C.c_uint32), ("init_random", C.c_uint32),
                 ("trace_mean_entropy", C.c_void_p), ("trace_canvas", C.c_void_p),
                 ("trace_h", C.c_void_p), ("trace_argmax", C.c_void_p), ("trace_conf", C.c_void_p),
-                ("trace_entropy", C.c_void_p)]
+                ("trace_entropy", C.c_void_p), ("trace_timeline", C.c_void_p)]
 
 
 class SynthParams(C.Structure):
@@ -228,15 +229,17 @@ def dg_canvas_loop(w, canvas, *, B: int, S: int, theta: float, y=None, denoise=N
                    seed: int = 0, max_passes: int = 48, stable_passes: int = 2,
                    stop_mode: int = STOP_OR, start_pass: int = 0, init_random: bool = True,
                    state=None, n_content: int = 50, s_content: float = 8.0, s_pad: float = 16.0,
-                   trace: bool = False, workspace=None, status=None, outputs: dict | None = None,
-                   stream=None) -> dict:
+                   trace: bool = False, timeline: bool = False, workspace=None, status=None,
+                   outputs: dict | None = None, stream=None) -> dict:
     """The whole denoising loop on the device (one graph launch, no host synchronisation).
 
     With y given (and denoise None) the built-in synthetic denoiser is used. `denoise`, if
     given, is a Python callable (canvas_ptr, pass_ptr, h_ptr, stream_handle) -> int that must
     enqueue capturable work on the stream it receives. `outputs` may hold preallocated
     argmax/conf/entropy tensors [B*S]; with the same tensors (and the same other arguments) a
-    repeated call reuses the captured graph.
+    repeated call reuses the captured graph. With timeline=True the result holds
+    "trace_timeline" [max_passes, 3, 2] (uint64 stored as int64): per pass, the device global
+    timer (ns) at the begin/end of the denoiser (built-in only), the head and the merge kernel.
     """
     dev = w.device
     R = B * S
@@ -274,6 +277,9 @@ def dg_canvas_loop(w, canvas, *, B: int, S: int, theta: float, y=None, denoise=N
         params.trace_argmax = _ptr(out["trace_argmax"]).value
         params.trace_conf = _ptr(out["trace_conf"]).value
         params.trace_entropy = _ptr(out["trace_entropy"]).value
+    if timeline:
+        out["trace_timeline"] = torch.empty(max_passes, DG_TL_KERNELS, 2, dtype=torch.int64, device=dev)
+        params.trace_timeline = _ptr(out["trace_timeline"]).value
     L = lib()
     keep = []
     if denoise is None:
@@ -294,6 +300,23 @@ def dg_canvas_loop(w, canvas, *, B: int, S: int, theta: float, y=None, denoise=N
                           _ptr(out["entropy"]), _ptr(ws), ws.numel(), _ptr(st), _stream(stream))
     _check(rc, "dg_canvas_loop")
     out["_keepalive"] = keep + [ws, desc, params]
+    return out
+
+
+def timeline_us(tl: torch.Tensor, passes: int) -> list:
+    """Per-pass kernel intervals in microseconds relative to the first recorded stamp, from a
+    loop's "trace_timeline": [{"denoise": (b, e) | None, "head": (b, e), "merge": (b, e)}, ...]."""
+    t = tl.detach().cpu().view(-1, DG_TL_KERNELS, 2).numpy().view("uint64")
+    valid = t[:passes][t[:passes, :, 1] > 0]
+    t0 = int(valid[:, 0].min()) if valid.size else 0
+    names = ("denoise", "head", "merge")
+    out = []
+    for p in range(passes):
+        row = {}
+        for k, n in enumerate(names):
+            b, e = int(t[p, k, 0]), int(t[p, k, 1])
+            row[n] = None if e == 0 else ((b - t0) / 1e3, (e - t0) / 1e3)
+        out.append(row)
     return out
 
 

@@ -160,6 +160,9 @@ struct Prepared {
     int path;
     DeviceInfo di;
     Layout L;
+    unsigned long long* timeline = nullptr;  // loop timeline (head stamps) or null
+    const int32_t* tl_pass = nullptr;
+    const int32_t* stop = nullptr;           // loop stop flag (device) or null
 };
 
 int prepare(const dg_head_desc* d, void* ws, size_t ws_bytes, Prepared* P, bool need_h = true) {
@@ -223,6 +226,9 @@ cudaError_t launch_head_only(const dg_head_desc* d, const Prepared& P, uint8_t* 
     a.crow_base = d->inv_temp * 1.4426950408889634f;
     a.partials = reinterpret_cast<float4*>(ws + P.L.off_partials);
     a.status = status;
+    a.timeline = P.timeline;
+    a.tl_pass = P.tl_pass;
+    a.stop = P.stop;
     a.w_scale = d->w_scale;
     a.h_scale = d->h_scale;
     cudaError_t e = cudaSuccess;
@@ -263,6 +269,7 @@ SelectArgs base_select(const dg_head_desc* d, const Prepared& P, uint8_t* ws, ui
     s.B = d->B;
     s.V = d->V;
     s.keep_k0 = -1;
+    s.inv_v = 1.0 / static_cast<double>(d->V);
     s.status = status;
     return s;
 }
@@ -284,7 +291,7 @@ using namespace dg;
 
 extern "C" {
 
-int dg_version(void) { return 100; }
+int dg_version(void) { return 101; }
 
 int dg_profile_next_head(void* start_event, void* stop_event) {
     if ((start_event == nullptr) != (stop_event == nullptr)) return DG_ERR_INVALID_ARG;
@@ -462,6 +469,7 @@ void copy_params(dg_loop_params* dst, const dg_loop_params& s) {
     dst->trace_argmax = s.trace_argmax;
     dst->trace_conf = s.trace_conf;
     dst->trace_entropy = s.trace_entropy;
+    dst->trace_timeline = s.trace_timeline;
 }
 
 void copy_synth(dg_synth_params* dst, const dg_synth_params& s) {
@@ -517,48 +525,61 @@ int build_loop_graph(LoopEntry* E, const Prepared& P) {
         return DG_ERR_CUDA;
     }
     int rc = DG_OK;
-    // The built-in denoiser feeding an E4M3 head quantises the rows it writes in the same kernel
-    // (the bf16 hidden states are still written to h_buffer).
-    const bool fuse_quant = k.fn == dg_synth_denoise && P.path == PATH_TC_E4M3_QUANT;
+    // The built-in denoiser is launched directly (with the timeline); in front of an E4M3 head it
+    // quantises the rows it writes in the same kernel (the bf16 hidden states are still written
+    // to h_buffer). With the built-in denoiser one graph iteration runs two passes, halving the
+    // per-iteration cost of the conditional node; once the loop has ended (ctl->stop) the
+    // kernels of the remaining pass do nothing. A caller's denoiser runs one pass per
+    // iteration, so it is never invoked after the loop ends.
+    const bool builtin = k.fn == dg_synth_denoise;
+    const bool fuse_quant = builtin && P.path == PATH_TC_E4M3_QUANT;
+    const int passes_per_iter = builtin ? 2 : 1;
     Prepared Ph = P;
-    if (fuse_quant) {
-        const dg_synth_params& sp = E->synth_user;
-        if (launch_synth_denoise(sp.desc, sp.y, sp.n_content, sp.s_content, sp.s_pad, k.canvas,
-                                 &ctl->pass, static_cast<uint16_t*>(k.h_buffer), sp.status, cs,
-                                 ws + P.L.off_qh, reinterpret_cast<float*>(ws + P.L.off_sch)) !=
-            cudaSuccess)
-            rc = DG_ERR_CUDA;
-        Ph.path = -PATH_TC_E4M3_QUANT;  // quantisation already done
-    } else {
-        void* user = (k.fn == dg_synth_denoise) ? static_cast<void*>(&E->synth_user) : k.user;
-        if (k.fn(user, k.canvas, &ctl->pass, k.h_buffer, reinterpret_cast<dg_stream_t>(cs)) != 0)
-            rc = DG_ERR_CUDA;
-    }
+    Ph.timeline = k.params.trace_timeline;
+    Ph.tl_pass = &ctl->pass;
+    Ph.stop = &ctl->stop;
+    if (fuse_quant) Ph.path = -PATH_TC_E4M3_QUANT;  // quantisation done by the denoiser
     const size_t hbytes = static_cast<size_t>(d->B) * d->S * d->d * elem_size(d->h_dtype);
-    if (rc == DG_OK && k.params.trace_h &&
-        launch_trace_copy(k.h_buffer, k.params.trace_h, hbytes, ctl, cs) != cudaSuccess)
-        rc = DG_ERR_CUDA;
-    if (rc == DG_OK && enqueue_head(d, Ph, ws, k.status, cs) != cudaSuccess) rc = DG_ERR_CUDA;
-    if (rc == DG_OK) {
-        SelectArgs s = base_select(d, P, ws, k.status);
-        set_stats(&s, P, ws, k.argmax, k.conf, k.entropy);
-        s.canvas_in = k.canvas;
-        s.canvas_out = k.canvas;
-        s.keep_k0 = k.params.keep_k0;
-        s.keep_sched = k.params.keep_sched;
-        s.seed = k.params.seed;
-        s.state = k.state;
-        s.rule = k.params.rule;
-        s.has_rule = 1;
-        s.ctl = ctl;
-        s.cond = handle;
-        s.set_cond = 1;
-        s.trace_mean_entropy = k.params.trace_mean_entropy;
-        s.trace_canvas = k.params.trace_canvas;
-        s.trace_argmax = k.params.trace_argmax;
-        s.trace_conf = k.params.trace_conf;
-        s.trace_entropy = k.params.trace_entropy;
-        if (launch_select(s, cs) != cudaSuccess) rc = DG_ERR_CUDA;
+    for (int it = 0; it < passes_per_iter && rc == DG_OK; ++it) {
+        if (builtin) {
+            const dg_synth_params& sp = E->synth_user;
+            if (launch_synth_denoise(sp.desc, sp.y, sp.n_content, sp.s_content, sp.s_pad, k.canvas,
+                                     &ctl->pass, static_cast<uint16_t*>(k.h_buffer), sp.status, cs,
+                                     fuse_quant ? ws + P.L.off_qh : nullptr,
+                                     fuse_quant ? reinterpret_cast<float*>(ws + P.L.off_sch)
+                                                : nullptr,
+                                     k.params.trace_timeline, &ctl->stop) != cudaSuccess)
+                rc = DG_ERR_CUDA;
+        } else if (k.fn(k.user, k.canvas, &ctl->pass, k.h_buffer,
+                        reinterpret_cast<dg_stream_t>(cs)) != 0) {
+            rc = DG_ERR_CUDA;
+        }
+        if (rc == DG_OK && k.params.trace_h &&
+            launch_trace_copy(k.h_buffer, k.params.trace_h, hbytes, ctl, cs) != cudaSuccess)
+            rc = DG_ERR_CUDA;
+        if (rc == DG_OK && enqueue_head(d, Ph, ws, k.status, cs) != cudaSuccess) rc = DG_ERR_CUDA;
+        if (rc == DG_OK) {
+            SelectArgs s = base_select(d, P, ws, k.status);
+            set_stats(&s, P, ws, k.argmax, k.conf, k.entropy);
+            s.canvas_in = k.canvas;
+            s.canvas_out = k.canvas;
+            s.keep_k0 = k.params.keep_k0;
+            s.keep_sched = k.params.keep_sched;
+            s.seed = k.params.seed;
+            s.state = k.state;
+            s.rule = k.params.rule;
+            s.has_rule = 1;
+            s.ctl = ctl;
+            s.cond = handle;
+            s.set_cond = 1;
+            s.trace_mean_entropy = k.params.trace_mean_entropy;
+            s.trace_canvas = k.params.trace_canvas;
+            s.trace_argmax = k.params.trace_argmax;
+            s.trace_conf = k.params.trace_conf;
+            s.trace_entropy = k.params.trace_entropy;
+            s.timeline = k.params.trace_timeline;
+            if (launch_select(s, cs) != cudaSuccess) rc = DG_ERR_CUDA;
+        }
     }
     cudaGraph_t captured = nullptr;
     if (cudaStreamEndCapture(cs, &captured) != cudaSuccess) rc = DG_ERR_CUDA;
@@ -607,8 +628,12 @@ extern "C" int dg_canvas_loop(const dg_head_desc* desc, int32_t* canvas, void* h
     Prepared P;
     int rc = prepare(desc, workspace, workspace_bytes, &P);
     if (rc != DG_OK) return rc;
-    if (denoise == dg_synth_denoise && (!user || static_cast<dg_synth_params*>(user)->desc == nullptr))
-        return DG_ERR_INVALID_ARG;
+    if (denoise == dg_synth_denoise) {
+        const dg_synth_params* sp = static_cast<const dg_synth_params*>(user);
+        if (!sp || !sp->desc || !sp->y) return DG_ERR_INVALID_ARG;
+        // the built-in denoiser writes bf16 hidden states from a bf16 or E4M3 head
+        if (sp->desc->w_dtype == DG_F32 || desc->h_dtype != DG_BF16) return DG_ERR_UNSUPPORTED;
+    }
 
     LoopKey key;
     std::memset(&key, 0, sizeof(key));
@@ -664,7 +689,8 @@ extern "C" int dg_canvas_loop(const dg_head_desc* desc, int32_t* canvas, void* h
     const int R = desc->B * desc->S;
     if (launch_loop_init(canvas, R, desc->S, desc->B, desc->V, params->seed, params->init_random ? 1 : 0,
                          state, params->start_pass > 0 ? 1 : 0, ctl,
-                         static_cast<int>(params->start_pass), r.max_passes, status, st) != cudaSuccess)
+                         static_cast<int>(params->start_pass), r.max_passes, status,
+                         params->trace_timeline, st) != cudaSuccess)
         return DG_ERR_CUDA;
     if (cudaGraphLaunch(E->exec, st) != cudaSuccess) return DG_ERR_CUDA;
     if (cudaEventRecord(E->done, st) != cudaSuccess) return DG_ERR_CUDA;

@@ -41,23 +41,22 @@ __device__ __forceinline__ Partial partial_empty() {
 }
 
 // Monoid merge: a (x) b. Associative up to rounding; equal maxima keep the lower index, so the
-// merged argmax is the lowest vocabulary index attaining the maximum.
+// merged argmax is the lowest vocabulary index attaining the maximum. The side with the larger
+// maximum ("hi") keeps its terms as they are (its rescale factor is exactly 1); only the other
+// side is rescaled, by 2^(lo.mx - hi.mx) <= 1 on the special-function unit.
 __device__ __forceinline__ Partial partial_merge(const Partial& a, const Partial& b) {
     if (b.s == 0.f) return a;
     if (a.s == 0.f) return b;
-    const float M = fmaxf(a.mx, b.mx);
-    const float da = a.mx - M, db = b.mx - M;
-    const float fa = exp2f(da), fb = exp2f(db);
+    const bool a_hi = (a.mx > b.mx) || (a.mx == b.mx && a.idx <= b.idx);
+    const Partial& hi = a_hi ? a : b;
+    const Partial& lo = a_hi ? b : a;
+    const float d = lo.mx - hi.mx;  // <= 0
+    const float e = ex2_fast(d);
     Partial r;
-    r.mx = M;
-    r.s = a.s * fa + b.s * fb;
-    r.u = fa * fmaf(a.s, da, a.u) + fb * fmaf(b.s, db, b.u);
-    if (a.mx > b.mx)
-        r.idx = a.idx;
-    else if (b.mx > a.mx)
-        r.idx = b.idx;
-    else
-        r.idx = min(a.idx, b.idx);
+    r.mx = hi.mx;
+    r.idx = hi.idx;
+    r.s = fmaf(lo.s, e, hi.s);
+    r.u = fmaf(e, fmaf(lo.s, d, lo.u), hi.u);
     return r;
 }
 
@@ -142,6 +141,20 @@ __host__ __device__ __forceinline__ uint64_t draw_key(uint64_t seed, uint32_t pa
 }
 
 constexpr uint32_t kInitPass = 0xFFFFFFFFu;
+
+// Exact x mod V for a 64-bit x and 1 <= V < 2^31, without the 64-bit integer division routine.
+// With x = hi * 2^32 + lo: t = (hi mod V) * 2^32 + lo has the same residue and t < V * 2^32, so
+// the quotient q = floor(t / V) < 2^32. q is estimated in double precision with inv_v = RN(1/V)
+// (relative error below 2^-50, so the estimate is within one of q) and the remainder corrected.
+__device__ __forceinline__ uint32_t mod_u64_by_u32(uint64_t x, uint32_t V, double inv_v) {
+    const uint32_t hi = static_cast<uint32_t>(x >> 32), lo = static_cast<uint32_t>(x);
+    const uint64_t t = (static_cast<uint64_t>(hi % V) << 32) | lo;
+    const uint64_t q = __double2ull_rz(__dmul_rn(__ull2double_rn(t), inv_v));
+    int64_t r = static_cast<int64_t>(t) - static_cast<int64_t>(q * V);
+    if (r < 0) r += V;
+    if (r >= static_cast<int64_t>(V)) r -= V;
+    return static_cast<uint32_t>(r);
+}
 
 __device__ __forceinline__ void flag_status(uint32_t* status, uint32_t bits) {
     if (status) atomicOr(status, bits);

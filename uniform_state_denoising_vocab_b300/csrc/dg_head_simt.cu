@@ -21,8 +21,10 @@ __global__ void __launch_bounds__(BM)
     head_simt_kernel(const float* __restrict__ h, const float* __restrict__ w, const HeadArgs args) {
     __shared__ __align__(16) float ws[BN][KC];
     const int t = threadIdx.x;
-    const int units = args.MB * args.n_groups;
     grid_dependency_wait();
+    const int units = (args.stop != nullptr && *args.stop != 0) ? 0 : args.MB * args.n_groups;
+    const int tl_pass = args.timeline != nullptr ? *args.tl_pass : 0;
+    if (units > 0) timeline_begin(args.timeline, tl_pass, DG_TL_HEAD);
     grid_launch_dependents();
     for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
         const int mb = unit % args.MB, grp = unit / args.MB;
@@ -79,6 +81,7 @@ __global__ void __launch_bounds__(BM)
         if (row_ok)
             args.partials[static_cast<size_t>(row) * args.n_groups + grp] = pack(row_state_partial(st));
     }
+    if (units > 0) timeline_end(args.timeline, tl_pass, DG_TL_HEAD);
 }
 
 }  // namespace

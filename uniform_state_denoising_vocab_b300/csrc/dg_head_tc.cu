@@ -68,7 +68,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int units = args.MB * args.n_groups;
     constexpr int KB_ELEMS = (KIND == 0) ? 64 : 128;  // elements per 128-byte K slice
 
     if (threadIdx.x == 0) {
@@ -95,6 +94,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
     grid_dependency_wait();  // the prologue above overlaps the previous kernel of the stream
+    // a pass after the loop has ended (second pass of a graph iteration) does no work
+    const int units = (args.stop != nullptr && *args.stop != 0) ? 0 : args.MB * args.n_groups;
+    const int tl_pass = args.timeline != nullptr ? *args.tl_pass : 0;
+    if (units > 0) timeline_begin(args.timeline, tl_pass, DG_TL_HEAD);
     grid_launch_dependents();
 
     if (warp == 0) {
@@ -221,6 +224,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
         tmem_dealloc(tmem_base, TMEM_COLS);
     }
+    if (units > 0) timeline_end(args.timeline, tl_pass, DG_TL_HEAD);
 }
 
 // cuTensorMapEncodeTiled from the driver, resolved once through the runtime.

@@ -82,7 +82,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const bool leader = rank == 0;
     const int pair = blockIdx.x >> 1;
     const int n_pairs = gridDim.x >> 1;
-    const int units = args.MB * args.n_groups;  // MB counts 256-row blocks here
     constexpr int KB_ELEMS = (KIND == 0) ? 64 : 128;
 
     if (threadIdx.x == 0) {
@@ -109,6 +108,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
     grid_dependency_wait();  // the prologue above overlaps the previous kernel of the stream
+    // a pass after the loop has ended (second pass of a graph iteration) does no work
+    const int units = (args.stop != nullptr && *args.stop != 0) ? 0 : args.MB * args.n_groups;
+    const int tl_pass = args.timeline != nullptr ? *args.tl_pass : 0;
+    if (units > 0) timeline_begin(args.timeline, tl_pass, DG_TL_HEAD);
     grid_launch_dependents();
 
     if (warp == 0) {
@@ -243,6 +246,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
         tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
+    if (units > 0) timeline_end(args.timeline, tl_pass, DG_TL_HEAD);
 }
 
 }  // namespace

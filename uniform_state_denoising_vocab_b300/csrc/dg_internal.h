@@ -43,6 +43,9 @@ struct HeadArgs {
     const float* w_scale;     // [V] or null
     float4* partials;         // [R][n_groups]: the partials of one row are contiguous
     uint32_t* status;         // sticky status word or null
+    unsigned long long* timeline;  // loop timeline (dg_loop_params.trace_timeline) or null
+    const int32_t* tl_pass;        // pass index for the timeline (device)
+    const int32_t* stop;           // loop mode: non-zero = the loop has ended, do nothing
 };
 
 // Programmatic dependent launch. Every kernel of a pass is launched with the programmatic
@@ -56,6 +59,22 @@ __device__ __forceinline__ void grid_dependency_wait() {
 __device__ __forceinline__ void grid_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+// Per-pass kernel timeline: the first CTA past its dependency wait sets `begin`, the last CTA to
+// finish sets `end` (atomic min / max of the device global timer, in ns). Thread 0 of each CTA.
+__device__ __forceinline__ unsigned long long globaltimer_now() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void timeline_begin(unsigned long long* tl, int pass, int kernel) {
+    if (tl != nullptr && threadIdx.x == 0)
+        atomicMin(tl + 2 * (static_cast<size_t>(pass) * DG_TL_KERNELS + kernel), globaltimer_now());
+}
+__device__ __forceinline__ void timeline_end(unsigned long long* tl, int pass, int kernel) {
+    if (tl != nullptr && threadIdx.x == 0)
+        atomicMax(tl + 2 * (static_cast<size_t>(pass) * DG_TL_KERNELS + kernel) + 1, globaltimer_now());
+}
+
 inline void set_pdl_attr(cudaLaunchAttribute* a) {
     a->id = cudaLaunchAttributeProgrammaticStreamSerialization;
     a->val.programmaticStreamSerializationAllowed = 1;
@@ -76,9 +95,9 @@ cudaError_t launch_head_simt(const float* h, const float* w, const HeadArgs& arg
 // Loop control block in the workspace (device).
 struct LoopCtl {
     int32_t pass;       // index of the pass about to run
-    uint32_t ticket;    // CTAs of the select kernel finished in this pass
+    uint32_t ticket;    // canvases of the merge kernel finished in this pass
     int32_t max_passes;
-    int32_t pad;
+    int32_t stop;       // set once the loop has ended: later passes of a graph iteration are no-ops
 };
 
 struct SelectArgs {
@@ -91,6 +110,7 @@ struct SelectArgs {
     uint8_t* kept;
     const int32_t* canvas_in;         // null: statistics only
     int32_t* canvas_out;
+    double inv_v;                     // RN(1 / V) for the exact draw modulo
     int keep_k;                       // fixed K when keep_k0 < 0
     int keep_k0;                      // >= 0: K_t = min(keep_k0 * (p + 1), S)
     const int32_t* keep_sched;        // optional [max_passes]
@@ -107,6 +127,7 @@ struct SelectArgs {
     int32_t* trace_argmax;            // optional [max_passes * R] (loop mode)
     float* trace_conf;
     float* trace_entropy;
+    unsigned long long* timeline;     // optional loop timeline
     uint32_t* status;
 };
 
@@ -120,18 +141,20 @@ cudaError_t launch_quant_rows(const uint16_t* h, int R, int d, uint8_t* q, float
 cudaError_t launch_loop_init(int32_t* canvas, int R, int S, int B, int V, uint64_t seed,
                              int init_random, dg_canvas_state* state, int keep_stable,
                              LoopCtl* ctl, int start_pass, int max_passes, uint32_t* status,
-                             cudaStream_t stream);
+                             unsigned long long* timeline, cudaStream_t stream);
 
 // Copy rows of one pass into a trace buffer at offset pass * bytes (pass read on device).
 cudaError_t launch_trace_copy(const void* src, void* dst, size_t bytes, const LoopCtl* ctl,
                               cudaStream_t stream);
 
-// Built-in synthetic denoiser. With q_out/scale_out non-null it also quantises each bf16 row
+// Built-in synthetic denoiser (stop: optional loop stop flag, non-zero = do nothing). With q_out/scale_out non-null it also quantises each bf16 row
 // it writes to E4M3 with the per-row absmax rule of launch_quant_rows (one kernel instead of two).
 cudaError_t launch_synth_denoise(const dg_head_desc* desc, const int32_t* y, int n_content,
                                  float s_content, float s_pad, const int32_t* canvas,
                                  const int32_t* pass, uint16_t* h_out, uint32_t* status,
                                  cudaStream_t stream, uint8_t* q_out = nullptr,
-                                 float* scale_out = nullptr);
+                                 float* scale_out = nullptr,
+                                 unsigned long long* timeline = nullptr,
+                                 const int32_t* stop = nullptr);
 
 }  // namespace dg

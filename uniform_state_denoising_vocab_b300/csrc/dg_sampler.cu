@@ -57,6 +57,7 @@ struct MergeSmem {
     float ent[kMaxRowsPerCta];
     int32_t arg[kMaxRowsPerCta];
     int32_t old[kMaxRowsPerCta];     // this CTA's slots' tokens before the pass
+    int32_t draw[kMaxRowsPerCta];    // this CTA's slots' re-randomised tokens for the pass
     float all_conf[1024];            // every slot of the canvas (gathered over the cluster)
     float warp_ent[32];              // CTA 0: per-warp sums of the entropy tree
     uint32_t changed[kMergeCluster]; // CTA 0: per-CTA "some slot changed" flags (pushed)
@@ -76,6 +77,8 @@ __global__ void __cluster_dims__(kMergeCluster, 1, 1) __maxnreg__(40)
     merge_select_kernel(const SelectArgs a) {
     __shared__ MergeSmem sm;
     grid_dependency_wait();
+    if (a.ctl != nullptr && *reinterpret_cast<const volatile int32_t*>(&a.ctl->stop) != 0)
+        return;  // the loop ended in an earlier pass of this graph iteration (uniform)
     const int b = blockIdx.x / kMergeCluster;
     const uint32_t c = cluster_ctarank();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -85,60 +88,77 @@ __global__ void __cluster_dims__(kMergeCluster, 1, 1) __maxnreg__(40)
     const int nrows = max(0, min(rpc, S - j0));
     const int base = b * S;
     const int p = a.ctl ? a.ctl->pass : static_cast<int>(a.pass);
-    const bool frozen = a.state != nullptr && a.state[b].done != 0;  // same in every CTA of b
+    timeline_begin(a.timeline, p, DG_TL_MERGE);
+    // Loads that do not depend on whether the canvas is frozen go out first: its state word,
+    // the old tokens of this CTA's slots and the partials of each warp's rows.
+    const int done = a.state != nullptr ? __ldcg(&a.state[b].done) : 0;  // same in every CTA of b
+    int old_tok = 0;
+    if (a.canvas_out && tid < nrows) old_tok = __ldcg(a.canvas_in + base + j0 + tid);
+    // CTA 0 applies the stop rule: its inputs are fetched now
+    dg_canvas_state st0 = {};
+    int max_passes = 0;
+    if (c == 0 && tid == 0) {
+        if (a.state != nullptr) st0 = a.state[b];
+        if (a.ctl != nullptr) max_passes = a.ctl->max_passes;
+    }
+    const bool frozen = done != 0;
+    int my_done = frozen ? 1 : 0;  // CTA 0 thread 0: this canvas is stopped after the pass
 
-    if (frozen) {
-        if (a.canvas_out && a.canvas_out != a.canvas_in)
-            for (int jj = tid; jj < nrows; jj += kMergeThreads)
-                a.canvas_out[base + j0 + jj] = a.canvas_in[base + j0 + jj];
-    } else {
-        // the old tokens of this CTA's slots, fetched while the partials are merged
-        int old_tok = 0;
-        if (a.canvas_out && tid < nrows) old_tok = a.canvas_in[base + j0 + tid];
-
-        for (int jj = warp; jj < nrows; jj += kMergeWarps) {
-            const int r = base + j0 + jj;
-            const float4* q = a.partials + static_cast<size_t>(r) * a.n_groups;
-            Partial acc = partial_empty();
-            // all of this lane's partials (groups lane, lane + 32, ...) in flight at once,
-            // then merged in increasing group order
-            for (int g0 = 0; g0 < a.n_groups; g0 += 4 * 32) {
-                float4 v[4];
+    // The rows are merged whether or not the canvas is frozen (the partials are this pass's), so
+    // that no load waits for the state word; a frozen canvas's outputs are left untouched.
+    for (int jj = warp; jj < nrows; jj += kMergeWarps) {
+        const int r = base + j0 + jj;
+        const float4* q = a.partials + static_cast<size_t>(r) * a.n_groups;
+        Partial acc = partial_empty();
+        // all of this lane's partials (groups lane, lane + 32, ...) in flight at once,
+        // then merged in increasing group order
+        for (int g0 = 0; g0 < a.n_groups; g0 += 4 * 32) {
+            float4 v[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int g = g0 + lane + 32 * i;
-                    v[i] = g < a.n_groups ? __ldcg(q + g) : pack(partial_empty());
-                }
+            for (int i = 0; i < 4; ++i) {
+                const int g = g0 + lane + 32 * i;
+                v[i] = g < a.n_groups ? __ldcg(q + g) : pack(partial_empty());
+            }
+            if (g0 == 0 && lane == 0 && a.canvas_out)  // integer work while the loads fly
+                sm.draw[jj] = static_cast<int32_t>(mod_u64_by_u32(
+                    draw_key(a.seed, static_cast<uint32_t>(p), static_cast<uint64_t>(r)),
+                    static_cast<uint32_t>(a.V), a.inv_v));
 #pragma unroll
-                for (int i = 0; i < 4; ++i) acc = partial_merge(acc, unpack(v[i]));
-            }
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const Partial o = shfl_xor_partial(acc, off);
-                acc = (lane & off) ? partial_merge(o, acc) : partial_merge(acc, o);
-            }
-            if (lane == 0) {
-                const float s = acc.s;
-                const float conf = 1.0f / s;
-                const float H = fmaxf(kLn2 * (log2f(s) - acc.u / s), 0.0f);
-                if (!(isfinite(s) && isfinite(acc.u) && isfinite(acc.mx) && s >= 1.0f - 1e-3f))
-                    flag_status(a.status, DG_ST_NONFINITE);
-                sm.conf[jj] = conf;
-                sm.ent[jj] = H;
-                sm.arg[jj] = acc.idx;
-                a.argmax[r] = acc.idx;
-                a.conf[r] = conf;
-                a.entropy[r] = H;
-                if (a.ctl) {
-                    const size_t tr = static_cast<size_t>(p) * a.R + r;
-                    if (a.trace_argmax) a.trace_argmax[tr] = acc.idx;
-                    if (a.trace_conf) a.trace_conf[tr] = conf;
-                    if (a.trace_entropy) a.trace_entropy[tr] = H;
-                }
-            }
+            for (int i = 0; i < 4; ++i) acc = partial_merge(acc, unpack(v[i]));
         }
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const Partial o = shfl_xor_partial(acc, off);
+            acc = (lane & off) ? partial_merge(o, acc) : partial_merge(acc, o);
+        }
+        if (lane == 0 && !frozen) {
+            const float s = acc.s;
+            sm.conf[jj] = 1.0f / s;
+            sm.ent[jj] = fmaxf(kLn2 * (log2f(s) - acc.u / s), 0.0f);
+            sm.arg[jj] = acc.idx;
+            if (!(isfinite(s) && isfinite(acc.u) && isfinite(acc.mx) && s >= 1.0f - 1e-3f))
+                flag_status(a.status, DG_ST_NONFINITE);
+        }
+    }
+
+    if (!frozen) {
         if (tid < nrows) sm.old[tid] = old_tok;
         cluster_sync();  // every CTA's statistics are in its shared memory
+
+        // this CTA's rows' statistics to the caller's arrays (and traces): after the barrier, so
+        // that its release does not wait for these stores
+        for (int jj = tid; jj < nrows; jj += kMergeThreads) {
+            const int r = base + j0 + jj;
+            a.argmax[r] = sm.arg[jj];
+            a.conf[r] = sm.conf[jj];
+            a.entropy[r] = sm.ent[jj];
+            if (a.ctl) {
+                const size_t tr = static_cast<size_t>(p) * a.R + r;
+                if (a.trace_argmax) a.trace_argmax[tr] = sm.arg[jj];
+                if (a.trace_conf) a.trace_conf[tr] = sm.conf[jj];
+                if (a.trace_entropy) a.trace_entropy[tr] = sm.ent[jj];
+            }
+        }
 
         // gather the canvas's confidences from the cluster; CTA 0 also sums the entropies with a
         // fixed-order tree: pairwise within each warp of 32 consecutive slots (xor butterfly),
@@ -187,10 +207,7 @@ __global__ void __cluster_dims__(kMergeCluster, 1, 1) __maxnreg__(40)
                 const int r = base + j;
                 const bool kp = rank < K;
                 const int oldt = sm.old[jj];
-                const int nw = kp ? sm.arg[jj]
-                                  : static_cast<int>(draw_key(a.seed, static_cast<uint32_t>(p),
-                                                              static_cast<uint64_t>(r)) %
-                                                     static_cast<uint64_t>(a.V));
+                const int nw = kp ? sm.arg[jj] : sm.draw[jj];
                 if (oldt < 0 || oldt >= a.V) flag_status(a.status, DG_ST_BAD_TOKEN);
                 if (a.trace_canvas && a.ctl) a.trace_canvas[static_cast<size_t>(p) * a.R + r] = oldt;
                 a.canvas_out[r] = nw;
@@ -209,14 +226,17 @@ __global__ void __cluster_dims__(kMergeCluster, 1, 1) __maxnreg__(40)
             meanH = sum / static_cast<float>(S);
         }
         cluster_sync();  // changed flags delivered; no CTA reads another's shared memory after this
-        if (c != 0) return;
+        if (c != 0) {
+            timeline_end(a.timeline, p, DG_TL_MERGE);
+            return;
+        }
         if (tid == 0) {
             if (a.mean_entropy) a.mean_entropy[b] = meanH;
             if (a.trace_mean_entropy && a.ctl) a.trace_mean_entropy[p * a.B + b] = meanH;
             if (a.canvas_out && a.state && a.has_rule) {
                 uint32_t any = 0;
                 for (int i = 0; i < kMergeCluster; ++i) any |= sm.changed[i];
-                dg_canvas_state st = a.state[b];
+                dg_canvas_state st = st0;
                 st.stable = any ? 0 : st.stable + 1;
                 const bool ent = meanH < a.rule.entropy_threshold;
                 const bool stb = st.stable >= a.rule.stable_passes;
@@ -232,9 +252,13 @@ __global__ void __cluster_dims__(kMergeCluster, 1, 1) __maxnreg__(40)
                                 (cap ? DG_REASON_CAP : 0);
                 }
                 a.state[b] = st;
+                my_done = st.done;
             }
         }
     }
+
+    if (frozen && a.canvas_out && a.canvas_out != a.canvas_in && tid < nrows)
+        a.canvas_out[base + j0 + tid] = old_tok;
 
     // loop mode: the last canvas of the pass advances the pass and sets the graph condition
     if (a.ctl && c == 0 && tid == 0) {
@@ -245,19 +269,21 @@ __global__ void __cluster_dims__(kMergeCluster, 1, 1) __maxnreg__(40)
         }
         if (t == static_cast<unsigned>(a.B) - 1u) {
             if (a.B > 1) __threadfence();
-            int all_done = 1;
-            if (a.state)
+            int all_done = a.state != nullptr ? my_done : 0;
+            if (a.state != nullptr && a.B > 1)
                 for (int bb = 0; bb < a.B; ++bb)
                     all_done &= (*reinterpret_cast<volatile int*>(&a.state[bb].done) != 0);
-            else
-                all_done = 0;
             a.ctl->ticket = 0;
             const int np = p + 1;
             a.ctl->pass = np;
-            if (a.set_cond)
-                cudaGraphSetConditional(a.cond, (!all_done && np < a.ctl->max_passes) ? 1u : 0u);
+            // the condition is 1 at every graph launch; it is only ever set to stop the loop
+            if (all_done || np >= max_passes) {
+                a.ctl->stop = 1;
+                if (a.set_cond) cudaGraphSetConditional(a.cond, 0u);
+            }
         }
     }
+    timeline_end(a.timeline, p, DG_TL_MERGE);
 }
 
 // Block-wide max of a non-negative value (blockDim.x a multiple of 32, at most 1024).
@@ -313,8 +339,15 @@ __global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ h, int d, ui
 
 __global__ void loop_init_kernel(int32_t* canvas, int S, int V, uint64_t seed, int init_random,
                                  dg_canvas_state* state, int keep_stable, LoopCtl* ctl,
-                                 int start_pass, int max_passes, uint32_t* status) {
+                                 int start_pass, int max_passes, uint32_t* status,
+                                 unsigned long long* timeline) {
     const int b = blockIdx.x;
+    if (timeline)
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < max_passes * DG_TL_KERNELS;
+             i += gridDim.x * blockDim.x) {
+            timeline[2 * i] = ~0ull;
+            timeline[2 * i + 1] = 0ull;
+        }
     for (int j = threadIdx.x; j < S; j += blockDim.x) {
         const int r = b * S + j;
         if (init_random) {
@@ -339,12 +372,14 @@ __global__ void loop_init_kernel(int32_t* canvas, int S, int V, uint64_t seed, i
             ctl->pass = start_pass;
             ctl->ticket = 0;
             ctl->max_passes = max_passes;
+            ctl->stop = 0;
         }
     }
 }
 
 __global__ void trace_copy_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
                                   size_t bytes, const LoopCtl* ctl) {
+    if (ctl->stop != 0) return;
     uint8_t* out = dst + static_cast<size_t>(ctl->pass) * bytes;
     const size_t n16 = bytes / 16;
     const uint4* s4 = reinterpret_cast<const uint4*>(src);
@@ -373,12 +408,15 @@ __global__ void synth_denoise_kernel(int dtype, const void* __restrict__ w, cons
                                      float s_content, float s_pad, const int32_t* __restrict__ canvas,
                                      const int32_t* __restrict__ pass, __nv_bfloat16* __restrict__ h,
                                      uint32_t* status, uint8_t* __restrict__ q,
-                                     float* __restrict__ qscale) {
+                                     float* __restrict__ qscale, unsigned long long* timeline,
+                                     const int32_t* stop) {
     __shared__ float red[32];
     grid_dependency_wait();
     grid_launch_dependents();
+    if (stop != nullptr && *stop != 0) return;
     const int r = blockIdx.x;
     const int t = pass[0] + 1;
+    timeline_begin(timeline, t - 1, DG_TL_DENOISE);
     const float at = fminf(1.0f, __fdiv_rn(static_cast<float>(2 + t), 10.0f));
     const float bt = 1.0f - at;
     const int yy = y[r], cc = canvas[r];
@@ -390,6 +428,7 @@ __global__ void synth_denoise_kernel(int dtype, const void* __restrict__ w, cons
             for (int k = threadIdx.x; k < d; k += blockDim.x) q[static_cast<size_t>(r) * d + k] = 0;
             if (threadIdx.x == 0) qscale[r] = 1.0f;
         }
+        timeline_end(timeline, t - 1, DG_TL_DENOISE);
         return;
     }
     float n2 = 0.f;
@@ -426,6 +465,7 @@ __global__ void synth_denoise_kernel(int dtype, const void* __restrict__ w, cons
         amax = block_max(amax, red);
         quant_row(hr, d, amax, q + static_cast<size_t>(r) * d, qscale + r);
     }
+    timeline_end(timeline, t - 1, DG_TL_DENOISE);
 }
 
 // Vectorised synthetic denoiser (same arithmetic as synth_denoise_kernel): one CTA of
@@ -480,14 +520,17 @@ __global__ void __launch_bounds__(kDenThreads)
                              int d, int V, const int32_t* __restrict__ y, int n_content,
                              float s_content, float s_pad, const int32_t* __restrict__ canvas,
                              const int32_t* __restrict__ pass, __nv_bfloat16* __restrict__ h,
-                             uint32_t* status, uint8_t* __restrict__ q, float* __restrict__ qscale) {
+                             uint32_t* status, uint8_t* __restrict__ q, float* __restrict__ qscale,
+                             unsigned long long* timeline, const int32_t* stop) {
     constexpr int EPC = 16 / ES;  // elements per 16-byte chunk
     __shared__ float red[8];
     grid_dependency_wait();
     grid_launch_dependents();
+    if (stop != nullptr && *stop != 0) return;
     const int r = blockIdx.x;
     const int tid = threadIdx.x;
     const int t = pass[0] + 1;
+    timeline_begin(timeline, t - 1, DG_TL_DENOISE);
     const int yy = y[r], cc = canvas[r];
     const float at = fminf(1.0f, __fdiv_rn(static_cast<float>(2 + t), 10.0f));
     const float bt = 1.0f - at;
@@ -500,6 +543,7 @@ __global__ void __launch_bounds__(kDenThreads)
             for (int k = tid; k < d; k += kDenThreads) q[static_cast<size_t>(r) * d + k] = 0;
             if (tid == 0) qscale[r] = 1.0f;
         }
+        timeline_end(timeline, t - 1, DG_TL_DENOISE);
         return;
     }
     const uint4* wy = reinterpret_cast<const uint4*>(w + static_cast<size_t>(yy) * d * ES);
@@ -557,7 +601,10 @@ __global__ void __launch_bounds__(kDenThreads)
                 dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
         }
     }
-    if (!q) return;
+    if (!q) {
+        timeline_end(timeline, t - 1, DG_TL_DENOISE);
+        return;
+    }
     if (__syncthreads_or(bad) && tid == 0) flag_status(status, DG_ST_NONFINITE);
     amax = block_max128(amax, red);
     uint8_t* qr = q + static_cast<size_t>(r) * d;
@@ -587,6 +634,7 @@ __global__ void __launch_bounds__(kDenThreads)
         }
     }
     if (tid == 0) qscale[r] = amax == 0.f ? 1.0f : __fdiv_rn(amax, 448.0f);
+    timeline_end(timeline, t - 1, DG_TL_DENOISE);
 }
 
 }  // namespace
@@ -621,10 +669,11 @@ cudaError_t launch_quant_rows(const uint16_t* h, int R, int d, uint8_t* q, float
 
 cudaError_t launch_loop_init(int32_t* canvas, int R, int S, int B, int V, uint64_t seed,
                              int init_random, dg_canvas_state* state, int keep_stable, LoopCtl* ctl,
-                             int start_pass, int max_passes, uint32_t* status, cudaStream_t stream) {
+                             int start_pass, int max_passes, uint32_t* status,
+                             unsigned long long* timeline, cudaStream_t stream) {
     (void)R;
     loop_init_kernel<<<B, 256, 0, stream>>>(canvas, S, V, seed, init_random, state, keep_stable, ctl,
-                                            start_pass, max_passes, status);
+                                            start_pass, max_passes, status, timeline);
     return cudaGetLastError();
 }
 
@@ -638,7 +687,8 @@ cudaError_t launch_trace_copy(const void* src, void* dst, size_t bytes, const Lo
 cudaError_t launch_synth_denoise(const dg_head_desc* desc, const int32_t* y, int n_content,
                                  float s_content, float s_pad, const int32_t* canvas,
                                  const int32_t* pass, uint16_t* h_out, uint32_t* status,
-                                 cudaStream_t stream, uint8_t* q_out, float* scale_out) {
+                                 cudaStream_t stream, uint8_t* q_out, float* scale_out,
+                                 unsigned long long* timeline, const int32_t* stop) {
     const int R = desc->B * desc->S;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(R);
@@ -659,17 +709,17 @@ cudaError_t launch_synth_denoise(const dg_head_desc* desc, const int32_t* y, int
             return cudaLaunchKernelEx(&cfg, synth_denoise_vec_kernel<2, MAXC>, wb, desc->w_scale,
                                       static_cast<int>(desc->S), static_cast<int>(desc->d),
                                       static_cast<int>(desc->V), y, n_content, s_content, s_pad,
-                                      canvas, pass, hb, status, q_out, scale_out);
+                                      canvas, pass, hb, status, q_out, scale_out, timeline, stop);
         return cudaLaunchKernelEx(&cfg, synth_denoise_vec_kernel<1, MAXC>, wb, desc->w_scale,
                                   static_cast<int>(desc->S), static_cast<int>(desc->d),
                                   static_cast<int>(desc->V), y, n_content, s_content, s_pad, canvas,
-                                  pass, hb, status, q_out, scale_out);
+                                  pass, hb, status, q_out, scale_out, timeline, stop);
     }
     cfg.blockDim = dim3(256);
     return cudaLaunchKernelEx(&cfg, synth_denoise_kernel, static_cast<int>(desc->w_dtype),
                               desc->w, desc->w_scale, static_cast<int>(desc->S),
                               static_cast<int>(desc->d), static_cast<int>(desc->V), y, n_content,
-                              s_content, s_pad, canvas, pass, hb, status, q_out, scale_out);
+                              s_content, s_pad, canvas, pass, hb, status, q_out, scale_out, timeline, stop);
 }
 
 }  // namespace dg
