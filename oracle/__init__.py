@@ -22,4 +22,6 @@ from .oracle import (  # noqa: F401
     sm64,
     step,
     synth_denoise,
+    temperature,
+    blocks,
 )

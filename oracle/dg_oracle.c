@@ -250,27 +250,40 @@ int32_t or_draw(uint64_t seed, uint32_t pass, uint64_t row, int64_t V) {
 /* ------------------------------------------------------------------------------------------
  * Keep / re-randomise for B canvases of S slots (rows r = b*S + slot):
  *   mean_entropy[b] = (1/S) sum_slots H;
- *   sort the slots of canvas b by (conf descending, slot ascending) and keep the first
- *   K = min(keep_k, S); kept slots take their argmax, the others key(seed, pass, r) mod V.
- *   kgap[b] = conf(rank K-1) - conf(rank K) when 0 < K < S, else +inf.
+ *   rank the slots of canvas b by their keep key, best first, ties to the lower slot, and keep
+ *   the first K = min(keep_k, S). The key is the confidence, larger first (keep_rule 0: keep the
+ *   slots the model is most confident about, "When to use a diffusion LLM", "How block
+ *   diffusion works"), or the entropy, smaller first (keep_rule 1: lock the lowest-entropy tokens
+ *   first, "DiffusionGemma 26B: How Google's Text Diffusion Model Generates Tokens in Parallel",
+ *   "Architecture Details").
+ *   Kept slots take their argmax. The others are re-drawn as key(seed, pass, row_offset + r) mod V
+ *   (uniform-state diffusion), or set to mask_id when mask_id >= 0 (the masked-diffusion
+ *   variant: re-mask instead of re-randomise, "DiffusionGemma: When Text Generation Stops Being
+ *   Sequential", introduction).
+ *   kgap[b] = |key(rank K-1) - key(rank K)| when 0 < K < S, else +inf.
  * ---------------------------------------------------------------------------------------- */
-static const double* g_conf_for_sort;
+static const double* g_key_for_sort;   /* larger is better */
 static int64_t g_base_for_sort;
 
-static int by_conf_then_slot(const void* pa, const void* pb) {
+static int by_key_then_slot(const void* pa, const void* pb) {
     int32_t a = *(const int32_t*)pa, b = *(const int32_t*)pb;
-    double ca = g_conf_for_sort[g_base_for_sort + a], cb = g_conf_for_sort[g_base_for_sort + b];
-    if (ca > cb) return -1;
-    if (ca < cb) return 1;
+    double ka = g_key_for_sort[g_base_for_sort + a], kb = g_key_for_sort[g_base_for_sort + b];
+    if (ka > kb) return -1;
+    if (ka < kb) return 1;
     return (a < b) ? -1 : (a > b);
 }
 
 int or_select(int64_t B, int64_t S, int64_t V, const int32_t* argmax, const double* conf,
               const double* entropy, int64_t keep_k, uint64_t seed, uint32_t pass,
+              int keep_rule, int64_t mask_id, uint64_t row_offset,
               int32_t* canvas_out, uint8_t* kept, double* mean_entropy, double* kgap) {
-    if (B < 0 || S <= 0 || V <= 0 || keep_k < 0) return -1;
+    if (B < 0 || S <= 0 || V <= 0 || keep_k < 0 || (keep_rule != 0 && keep_rule != 1) ||
+        mask_id >= V)
+        return -1;
     int32_t* order = (int32_t*)malloc(sizeof(int32_t) * (size_t)S);
-    if (!order) return -2;
+    double* key = (double*)malloc(sizeof(double) * (size_t)(B * S));
+    if (!order || !key) { free(order); free(key); return -2; }
+    for (int64_t r = 0; r < B * S; r++) key[r] = keep_rule == 0 ? conf[r] : -entropy[r];
     int64_t K = keep_k < S ? keep_k : S;
     for (int64_t b = 0; b < B; b++) {
         int64_t base = b * S;
@@ -278,20 +291,22 @@ int or_select(int64_t B, int64_t S, int64_t V, const int32_t* argmax, const doub
         for (int64_t j = 0; j < S; j++) sum += entropy[base + j];
         mean_entropy[b] = sum / (double)S;
         for (int64_t j = 0; j < S; j++) order[j] = (int32_t)j;
-        g_conf_for_sort = conf;
+        g_key_for_sort = key;
         g_base_for_sort = base;
-        qsort(order, (size_t)S, sizeof(int32_t), by_conf_then_slot);
+        qsort(order, (size_t)S, sizeof(int32_t), by_key_then_slot);
         for (int64_t j = 0; j < S; j++) kept[base + j] = 0;
         for (int64_t j = 0; j < K; j++) kept[base + order[j]] = 1;
         if (kgap)
-            kgap[b] = (K > 0 && K < S) ? conf[base + order[K - 1]] - conf[base + order[K]]
-                                       : INFINITY;
+            kgap[b] = (K > 0 && K < S) ? key[base + order[K - 1]] - key[base + order[K]] : INFINITY;
         for (int64_t j = 0; j < S; j++) {
             int64_t r = base + j;
-            canvas_out[r] = kept[r] ? argmax[r] : or_draw(seed, pass, (uint64_t)r, V);
+            canvas_out[r] = kept[r] ? argmax[r]
+                          : mask_id >= 0 ? (int32_t)mask_id
+                                         : or_draw(seed, pass, row_offset + (uint64_t)r, V);
         }
     }
     free(order);
+    free(key);
     return 0;
 }
 

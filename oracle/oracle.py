@@ -55,7 +55,8 @@ def _L():
         lib.or_head_stats.argtypes = [i64, i64, i64, C.c_int, vp, vp, vp, vp, dbl, vp, i64,
                                       vp, vp, vp, vp]
         lib.or_head_stats.restype = C.c_int
-        lib.or_select.argtypes = [i64, i64, i64, vp, vp, vp, i64, u64, u32, vp, vp, vp, vp]
+        lib.or_select.argtypes = [i64, i64, i64, vp, vp, vp, i64, u64, u32, C.c_int, i64, u64,
+                                  vp, vp, vp, vp]
         lib.or_select.restype = C.c_int
         lib.or_sm64.argtypes = [u64]
         lib.or_sm64.restype = u64
@@ -171,8 +172,10 @@ def head_stats(R: int, d: int, V: int, dtype, h, w, h_scale=None, w_scale=None,
 
 
 def select(B: int, S: int, V: int, argmax, conf, entropy, keep_k: int, seed: int,
-           pass_: int) -> dict:
-    """Mean entropy, top-K keep by (conf desc, slot asc), and the re-randomised canvas."""
+           pass_: int, keep_rule: int = 0, mask_id: int = -1, row_offset: int = 0) -> dict:
+    """Mean entropy, top-K keep by (conf desc, slot asc) -- or by (entropy asc, slot asc) with
+    keep_rule=1 -- and the new canvas: re-drawn key(seed, pass, row_offset + r) mod V, or mask_id
+    when mask_id >= 0 (masked-diffusion variant)."""
     a = _c(argmax, np.int32)
     cf = _c(conf, np.float64)
     en = _c(entropy, np.float64)
@@ -181,7 +184,8 @@ def select(B: int, S: int, V: int, argmax, conf, entropy, keep_k: int, seed: int
     out = {"canvas": np.empty(R, np.int32), "kept": np.empty(R, np.uint8),
            "mean_entropy": np.empty(B, np.float64), "kgap": np.empty(B, np.float64)}
     rc = _L().or_select(B, S, V, _p(a), _p(cf), _p(en), int(keep_k), C.c_uint64(seed),
-                        C.c_uint32(pass_ & 0xFFFFFFFF), _p(out["canvas"]), _p(out["kept"]),
+                        C.c_uint32(pass_ & 0xFFFFFFFF), int(keep_rule), int(mask_id),
+                        C.c_uint64(row_offset), _p(out["canvas"]), _p(out["kept"]),
                         _p(out["mean_entropy"]), _p(out["kgap"]))
     if rc != 0:
         raise RuntimeError(f"or_select failed: {rc}")
@@ -189,7 +193,8 @@ def select(B: int, S: int, V: int, argmax, conf, entropy, keep_k: int, seed: int
 
 
 def step(B: int, S: int, V: int, d: int, dtype, h, w, keep_k: int, seed: int, pass_: int,
-         h_scale=None, w_scale=None, inv_temp: float = 1.0) -> dict:
+         h_scale=None, w_scale=None, inv_temp: float = 1.0, keep_rule: int = 0,
+         mask_id: int = -1, row_offset: int = 0) -> dict:
     """One canvas pass. For an E4M3 head given bf16 h, h is first quantised per row."""
     dt = _DT[dtype]
     out = {}
@@ -198,7 +203,8 @@ def step(B: int, S: int, V: int, d: int, dtype, h, w, keep_k: int, seed: int, pa
         h, h_scale = q, sc
         out["q_h"], out["sc_h"] = q, sc
     st = head_stats(B * S, d, V, dt, h, w, h_scale, w_scale, inv_temp=inv_temp)
-    sel = select(B, S, V, st["argmax"], st["conf"], st["entropy"], keep_k, seed, pass_)
+    sel = select(B, S, V, st["argmax"], st["conf"], st["entropy"], keep_k, seed, pass_,
+                 keep_rule=keep_rule, mask_id=mask_id, row_offset=row_offset)
     out.update(st)
     out.update(sel)
     return out
@@ -224,10 +230,21 @@ def synth_denoise(B: int, S: int, d: int, V: int, w_dtype, w, y, canvas, pass_: 
 # ---------------------------------------------------------------------------------------------
 # the denoising loop
 # ---------------------------------------------------------------------------------------------
+def temperature(p: int, max_passes: int, temp_start: float, temp_end: float) -> float:
+    """Sampling temperature of pass p (0-based) on a schedule decaying linearly from temp_start
+    at the first pass to temp_end at the last possible pass (0.8 -> 0.4 on the pages:
+    "DiffusionGemma 26B: How Google's Text Diffusion Model Generates Tokens in Parallel",
+    "Architecture Details"; "When to use a diffusion LLM", "Appendix: Methodology / Decoding")."""
+    if max_passes <= 1:
+        return float(temp_start)
+    return temp_start + (temp_end - temp_start) * p / (max_passes - 1)
+
+
 def loop(B: int, S: int, V: int, d: int, dtype, w, denoise, *, theta: float,
          stable_passes: int = 2, max_passes: int = 48, keep_k0: int = 32, keep_sched=None,
          seed: int = 0, canvas0=None, start_pass: int = 0, stable0=None, stop_and: bool = False,
-         w_scale=None, record: bool = False) -> dict:
+         w_scale=None, record: bool = False, temp_start=None, temp_end=None, keep_rule: int = 0,
+         mask_id: int = -1, row_offset: int = 0) -> dict:
     """Run the sampler loop; each canvas stops on its own and is frozen after it stops.
 
     denoise(canvas: int32[R], p: int) -> hidden states for the head: float32 [R*d] for an fp32
@@ -235,13 +252,19 @@ def loop(B: int, S: int, V: int, d: int, dtype, w, denoise, *, theta: float,
     Rules after pass p (OR by default; stop_and=True requires entropy AND stability):
       entropy: mean H < theta; stable: canvas unchanged for `stable_passes` consecutive passes;
       cap: p + 1 == max_passes.
+    With temp_start/temp_end the statistics of pass p are those of softmax(l / T_p) (see
+    temperature()). keep_rule 1 keeps the lowest-entropy slots; mask_id >= 0 is the masked
+    variant (the canvas starts all-mask and non-kept slots are re-masked); row_offset shifts the
+    rows of the re-draw key (a block's offset in a block-autoregressive run).
     """
     dt = _DT[dtype]
     R = B * S
-    if canvas0 is None:
-        c = draw(seed, INIT_PASS, np.arange(R), V)
-    else:
+    if canvas0 is not None:
         c = _c(canvas0, np.int32).copy()
+    elif mask_id >= 0:
+        c = np.full(R, mask_id, np.int32)
+    else:
+        c = draw(seed, INIT_PASS, row_offset + np.arange(R, dtype=np.uint64), V)
     stable = np.zeros(B, np.int64) if stable0 is None else np.array(stable0, np.int64)
     done = np.zeros(B, bool)
     passes = np.zeros(B, np.int32)
@@ -253,7 +276,10 @@ def loop(B: int, S: int, V: int, d: int, dtype, w, denoise, *, theta: float,
         t = p + 1
         K = int(keep_sched[p]) if keep_sched is not None else min(keep_k0 * t, S)
         h = denoise(c.copy(), p)
-        res = step(B, S, V, d, dt, h, w, K, seed, p, w_scale=w_scale)
+        inv_temp = 1.0 if temp_start is None else 1.0 / temperature(p, max_passes, temp_start,
+                                                                   temp_end)
+        res = step(B, S, V, d, dt, h, w, K, seed, p, w_scale=w_scale, inv_temp=inv_temp,
+                   keep_rule=keep_rule, mask_id=mask_id, row_offset=row_offset)
         if record:
             trace.append({"pass": p, "canvas_in": c.copy(), "h": h, **res})
         for b in range(B):
@@ -277,3 +303,26 @@ def loop(B: int, S: int, V: int, d: int, dtype, w, denoise, *, theta: float,
             break
     return {"canvas": c, "passes": passes, "reason": reason, "mean_entropy": last_meanH,
             "argmax": last_argmax, "stable": stable, "trace": trace}
+
+
+def blocks(n_blocks: int, B: int, S: int, V: int, d: int, dtype, w, y_blocks, *, theta: float,
+           n_content: int, s_content: float, s_pad: float, w_scale=None, **loop_kw) -> dict:
+    """Block-autoregressive generation with the synthetic denoiser: block i runs the whole
+    sampler loop on a fresh canvas with its own targets y_blocks[i] and its re-draw rows offset
+    by i*B*S, then commits its final canvas, and block i+1 starts ("DiffusionGemma 26B: How
+    Google's Text Diffusion Model Generates Tokens in Parallel", "How Diffusion Changes the
+    Equation": the model generates block by block; "When to use a diffusion LLM", "How block
+    diffusion works"). Returns the committed tokens [n_blocks*B*S] and per-block passes/reasons."""
+    R = B * S
+    yb = _c(y_blocks, np.int32).reshape(n_blocks, R)
+    tokens = np.empty(n_blocks * R, np.int32)
+    passes = np.empty((n_blocks, B), np.int32)
+    reason = np.empty((n_blocks, B), np.int32)
+    for i in range(n_blocks):
+        den = (lambda yy: lambda c, p: synth_denoise(B, S, d, V, dtype, w, yy, c, p, n_content,
+                                                     s_content, s_pad, w_scale=w_scale))(yb[i])
+        res = loop(B, S, V, d, dtype, w, den, theta=theta, w_scale=w_scale, row_offset=i * R,
+                   **loop_kw)
+        tokens[i * R:(i + 1) * R] = res["canvas"]
+        passes[i], reason[i] = res["passes"], res["reason"]
+    return {"tokens": tokens, "passes": passes, "reason": reason}

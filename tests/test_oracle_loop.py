@@ -123,3 +123,74 @@ def test_resume_matches_straight_run(orc, head):
                    canvas0=mid, start_pass=k, stable0=[stable])
     assert np.array_equal(res["canvas"], full["canvas"])
     assert list(res["passes"]) == list(full["passes"])
+
+
+def test_temperature_schedule_per_pass(orc):
+    """With a temperature schedule the statistics of pass p are those of softmax(l / T_p),
+    T_p falling linearly from 0.8 at the first pass to 0.4 at the last possible pass: every slot
+    has two-level logits (L at one id, 0 elsewhere), so each pass's mean entropy is the closed
+    form at T_p."""
+    import mpmath
+    Vt, dt, St, L, P = 50, 8, 4, 2.0, 6
+    w = np.zeros((Vt, dt), np.float32)
+    w[7, 0] = 1.0
+    wb = _bf16(w.reshape(-1))
+    h = _bf16(np.tile(np.array([L] + [0.0] * (dt - 1), np.float32), St))
+    assert orc.temperature(0, P, 0.8, 0.4) == 0.8 and abs(orc.temperature(P - 1, P, 0.8, 0.4) - 0.4) < 1e-15
+    res = orc.loop(1, St, Vt, dt, "bf16", wb, lambda c, p: h, theta=1e-9, keep_k0=0, seed=4,
+                   max_passes=P, temp_start=0.8, temp_end=0.4, record=True)
+    assert res["passes"][0] == P
+    for tr in res["trace"]:
+        T = 0.8 - 0.4 * tr["pass"] / (P - 1)
+        x = mpmath.mpf(L) / T
+        Z = mpmath.e ** x + (Vt - 1)
+        H = float(mpmath.log(Z) - x * mpmath.e ** x / Z)
+        assert abs(tr["mean_entropy"][0] - H) < 1e-12
+        assert (tr["argmax"] == 7).all()
+
+
+def test_masked_variant_loop(orc, head):
+    """Masked variant: the canvas starts all-mask, and a pass keeping every slot sets every slot
+    to its argmax; with nothing kept the canvas stays all-mask and the loop ends by stability."""
+    mask = V - 1
+    h = _const_h(1.0)
+    st = orc.step(B, S, V, d, "bf16", h, head, S, 0, 0)
+    res = orc.loop(B, S, V, d, "bf16", head, lambda c, p: h, theta=1e-9, keep_k0=S, seed=1,
+                   mask_id=mask, record=True)
+    assert (res["trace"][0]["canvas_in"] == mask).all()
+    assert np.array_equal(res["canvas"], st["argmax"])
+    res = orc.loop(B, S, V, d, "bf16", head, lambda c, p: h, theta=1e-9, keep_k0=0, seed=1,
+                   mask_id=mask)
+    assert (res["canvas"] == mask).all() and res["passes"][0] == 2 and res["reason"][0] == 2
+
+
+def test_row_offset_initial_canvas(orc, head):
+    """A block's row offset shifts the rows of the initial random canvas's key as well."""
+    from test_oracle_select import _py_key
+    h = _const_h(0.01)
+    off = 5 * B * S
+    res = orc.loop(B, S, V, d, "bf16", head, lambda c, p: h, theta=0.05, keep_k0=0, seed=2,
+                   max_passes=1, row_offset=off, record=True)
+    want = [_py_key(2, 0xFFFFFFFF, off + r) % V for r in range(B * S)]
+    assert list(res["trace"][0]["canvas_in"]) == want
+
+
+def test_block_driver_offsets(orc, head):
+    """Block i of a block-autoregressive run keys its draws with rows offset by i*B*S: with one
+    pass and nothing kept, every committed token of block i is key(seed, 0, i*B*S + r) mod V
+    (independent Python restatement of the key); and block i equals a single loop with that
+    offset and block i's targets."""
+    from test_oracle_select import _py_key
+    n, R = 3, B * S
+    rng = np.random.default_rng(21)
+    yb = rng.integers(0, V, n * R).astype(np.int32)
+    kw = dict(theta=0.05, n_content=5, s_content=8.0, s_pad=16.0)
+    res = orc.blocks(n, B, S, V, d, "bf16", head, yb, keep_k0=0, seed=9, max_passes=1, **kw)
+    assert list(res["tokens"]) == [_py_key(9, 0, r) % V for r in range(n * R)]
+    res = orc.blocks(n, B, S, V, d, "bf16", head, yb, keep_k0=4, seed=9, **kw)
+    for i in range(n):
+        den = lambda c, p, yy=yb[i * R:(i + 1) * R]: orc.synth_denoise(B, S, d, V, "bf16", head, yy,
+                                                                    c, p, 5, 8.0, 16.0)
+        one = orc.loop(B, S, V, d, "bf16", head, den, theta=0.05, keep_k0=4, seed=9, row_offset=i * R)
+        assert np.array_equal(res["tokens"][i * R:(i + 1) * R], one["canvas"])
+        assert res["passes"][i][0] == one["passes"][0]

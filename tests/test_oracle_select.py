@@ -114,3 +114,50 @@ def test_synth_denoise_properties(orc):
     # zero head rows give h = 0
     hz = orc.synth_denoise(1, 1, d, V, "bf16", np.zeros(V * d, np.uint16), [0], [1], 0, 1, 8, 16)
     assert not hz.any()
+
+
+def _brute_keep_entropy(H, K):
+    """The kept set under (entropy asc, slot asc): every kept slot beats every dropped slot."""
+    S = len(H)
+    found = [set(sub) for sub in itertools.combinations(range(S), K)
+             if all((H[i] < H[j]) or (H[i] == H[j] and i < j)
+                    for i in sub for j in range(S) if j not in sub)]
+    assert len(found) == 1
+    return found[0]
+
+
+@pytest.mark.parametrize("S", [1, 3, 6, 9])
+def test_entropy_keep_brute_force_with_ties(orc, S):
+    rng = np.random.default_rng(100 + S)
+    for trial in range(5):
+        H = rng.integers(0, 3, S).astype(np.float64) / 2.0 if trial % 2 else rng.random(S) * 4
+        conf = rng.random(S)    # must be ignored by the entropy rule
+        for K in range(0, S + 2):
+            res = orc.select(1, S, 777, np.arange(S), conf, H, K, 3, 1, keep_rule=1)
+            kept = {i for i in range(S) if res["kept"][i]}
+            assert len(kept) == min(K, S)
+            if 0 < K < S:
+                assert kept == _brute_keep_entropy(list(H), K)
+                order = sorted(range(S), key=lambda j: (H[j], j))
+                assert abs(res["kgap"][0] - (H[order[K]] - H[order[K - 1]])) < 1e-15
+
+
+def test_masked_variant_and_row_offset(orc):
+    B, S, V = 2, 9, 40
+    rng = np.random.default_rng(6)
+    argmax = rng.integers(0, V, B * S).astype(np.int32)
+    conf, H = rng.random(B * S), rng.random(B * S)
+    # re-mask: dropped slots take the mask id, kept slots their argmax
+    res = orc.select(B, S, V, argmax, conf, H, 4, 7, 2, mask_id=V - 1)
+    assert np.array_equal(res["canvas"], np.where(res["kept"] == 1, argmax, V - 1))
+    # a row offset shifts the key's row index: rows r are drawn as key(seed, pass, off + r)
+    off = 3 * B * S + 5
+    res = orc.select(B, S, V, argmax, conf, H, 4, 7, 2, row_offset=off)
+    for r in range(B * S):
+        want = argmax[r] if res["kept"][r] else _py_key(7, 2, off + r) % V
+        assert res["canvas"][r] == want
+    # invalid rules are refused
+    with pytest.raises(RuntimeError):
+        orc.select(B, S, V, argmax, conf, H, 4, 7, 2, keep_rule=2)
+    with pytest.raises(RuntimeError):
+        orc.select(B, S, V, argmax, conf, H, 4, 7, 2, mask_id=V)

@@ -115,6 +115,24 @@ def test_two_level_closed_form(orc, L, V):
         assert got["entropy"][0] < 1e-20
 
 
+@pytest.mark.parametrize("T", [0.4, 0.8, 2.5])
+def test_temperature_closed_forms(orc, T):
+    # statistics of softmax(l / T): the two-level closed form with L / T, and uniform logits
+    # stay uniform (H = ln V, conf = 1/V) at any temperature
+    V, d, j0, L = 1000, 4, 17, 3.0
+    h = np.array([1.0, 0, 0, 0], np.float32)
+    w = np.zeros((V, d), np.float32)
+    w[j0, 0] = L
+    got = orc.head_stats(1, d, V, "f32", h, w.reshape(-1), inv_temp=1.0 / T)
+    x = mpmath.mpf(L) / mpmath.mpf(T)
+    Z = mpmath.e ** x + (V - 1)
+    assert got["argmax"][0] == j0
+    assert abs(got["conf"][0] - float(mpmath.e ** x / Z)) <= 1e-12
+    assert abs(got["entropy"][0] - float(mpmath.log(Z) - x * mpmath.e ** x / Z)) <= 1e-12
+    u = orc.head_stats(1, d, V, "f32", h, np.zeros(V * d, np.float32), inv_temp=1.0 / T)
+    assert abs(u["entropy"][0] - np.log(V)) <= 1e-12 and abs(u["conf"][0] - 1.0 / V) <= 1e-15
+
+
 def test_bounds_and_permutation_invariance(orc):
     rng = np.random.default_rng(5)
     R, d, V = 16, 12, 333
