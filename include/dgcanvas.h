@@ -77,6 +77,14 @@ enum {
 /* Stop reasons (bitmask of every rule true at the stopping pass). */
 enum { DG_REASON_ENTROPY = 1, DG_REASON_STABLE = 2, DG_REASON_CAP = 4 };
 enum { DG_STOP_OR = 0, DG_STOP_AND = 1 };
+/* Which slots a pass keeps: the K most confident (max-prob), or the K lowest-entropy ones
+   ("lowest-entropy tokens locked first", dev.to page, "Architecture Details"); ties to the lower
+   slot either way. */
+enum { DG_KEEP_CONFIDENCE = 0, DG_KEEP_ENTROPY = 1 };
+/* What the other slots become: a uniform re-draw key(seed, pass, row) mod V (uniform-state
+   diffusion), or a fixed mask token (the masked-diffusion variant: "DiffusionGemma: When Text
+   Generation Stops Being Sequential" (laura-martel.com), introduction). */
+enum { DG_REDRAW_UNIFORM = 0, DG_REDRAW_MASK = 1 };
 
 /*
  * The vocabulary head and the hidden states of one batch of canvases.
@@ -112,12 +120,17 @@ typedef struct {
     int32_t reserved[2];
 } dg_canvas_state;
 
-/* Stop rule parameters for dg_canvas_step with a state, and for dg_canvas_loop. */
+/* The rules of a pass: its stop test (used by dg_canvas_step with a state, and by
+   dg_canvas_loop) and its keep / re-draw variant (used by every pass given a rule; a NULL rule
+   means DG_KEEP_CONFIDENCE and DG_REDRAW_UNIFORM). A zero-initialised tail selects the defaults. */
 typedef struct {
     int32_t max_passes;        /* pass cap (48 in the pages) */
     float entropy_threshold;   /* stop when mean H < threshold (nats) */
     int32_t stable_passes;     /* stop when unchanged for this many consecutive passes (2) */
     int32_t stop_mode;         /* DG_STOP_OR or DG_STOP_AND */
+    int32_t keep_rule;         /* DG_KEEP_CONFIDENCE (default) or DG_KEEP_ENTROPY */
+    int32_t redraw_mode;       /* DG_REDRAW_UNIFORM (default) or DG_REDRAW_MASK */
+    int32_t mask_id;           /* the mask token, in [0, V), with DG_REDRAW_MASK */
 } dg_stop_rule;
 
 /* Bytes of workspace a call with this descriptor needs (same for stats/step/loop). */
@@ -139,7 +152,8 @@ DG_API int dg_canvas_stats(const dg_head_desc* desc, int32_t* argmax, float* con
  * canvas_in == canvas_out is allowed. kept [B*S] (uint8 0/1) and the statistics outputs may be
  * NULL. If `state` (device, [B]) and `rule` (host) are given, the pass also applies the stop
  * test: it updates stable/done/passes/reason, and canvases already done are left unchanged
- * (copied to canvas_out). rule may only be NULL when state is NULL.
+ * (copied to canvas_out). rule may only be NULL when state is NULL; without a state only its
+ * keep / re-draw variant is used.
  */
 DG_API int dg_canvas_step(const dg_head_desc* desc, const int32_t* canvas_in, int32_t* canvas_out,
                    int32_t keep_k, uint64_t seed, uint32_t pass, int32_t* argmax, float* conf,
@@ -181,9 +195,17 @@ DG_API int dg_synth_denoise(void* user, const int32_t* canvas, const int32_t* pa
  * conditional WHILE node runs [denoise -> (quantise) -> statistics -> keep/re-randomise/stop]
  * until every canvas has stopped or max_passes is reached.
  *   canvas [B*S]: the canvas (in/out). If init_random, it is first overwritten with
- *     key(seed, 0xFFFFFFFF, r) mod V.
+ *     key(seed, 0xFFFFFFFF, row_offset + r) mod V (with DG_REDRAW_MASK: the mask token).
  *   h_buffer: device [B*S, d] buffer the denoiser writes (desc->h must equal it).
  *   K_t = keep_sched ? keep_sched[p] : min(keep_k0 * (p + 1), S) for 0-based pass p.
+ *   Re-draws of pass p use key(seed, p, row_offset + r) (a block's offset in a
+ *   block-autoregressive run; 0 otherwise).
+ *   With temp_start > 0 the statistics of pass p are those of softmax(l / T_p), l the logits of
+ *   the descriptor (inv_temp included), T_p = temp_start + (temp_end - temp_start) * p /
+ *   (max_passes - 1) in fp32 (temp_start alone when max_passes = 1): the 0.8 -> 0.4 anneal of
+ *   the dev.to page, "Architecture Details", and the devengoratela.com page, "Appendix:
+ *   Methodology / Decoding". The argmax is unaffected; confidence, entropy, the keep order and
+ *   the entropy stop test are.
  *   state [B] (device): on entry `stable` is the resume count when start_pass > 0 (and is
  *     reset to 0 otherwise); on exit it holds passes/reason/mean_entropy per canvas.
  *   argmax/conf/entropy: optional device outputs of the last pass that ran.
@@ -211,6 +233,8 @@ typedef struct {
        passes that did not run, and of the built-in denoiser when the caller supplies its own,
        stay at (UINT64_MAX, 0). Costs one branch per CTA when NULL. */
     unsigned long long* trace_timeline;
+    float temp_start, temp_end;  /* temperature schedule; temp_start = 0: none */
+    uint64_t row_offset;         /* added to the row index of every re-draw key */
 } dg_loop_params;
 
 /* Kernels recorded in dg_loop_params.trace_timeline. */
@@ -221,6 +245,23 @@ DG_API int dg_canvas_loop(const dg_head_desc* desc, int32_t* canvas, void* h_buf
                    dg_canvas_state* state, int32_t* argmax, float* conf, float* entropy,
                    void* workspace, size_t workspace_bytes, uint32_t* status,
                    dg_stream_t stream);
+
+/*
+ * Block-autoregressive generation with the built-in synthetic denoiser: block i (0-based) runs
+ * the whole loop (dg_canvas_loop with init_random, start_pass 0 and row_offset =
+ * params->row_offset + i*B*S) on a fresh canvas with targets y_blocks[i*B*S ...], then commits its
+ * final canvas to tokens_out[i*B*S ...] and its per-canvas state to states_out[i*B ...]; block
+ * i+1 starts after it, on the same stream, with no host synchronisation. The model would condition
+ * each block on the committed ones through its KV cache; the synthetic denoiser does not.
+ *   y_work [B*S], canvas [B*S], state [B]: device work buffers (written); desc->h == h_buffer.
+ *   One captured loop graph serves every block (only y_work's contents and the row offset change).
+ */
+DG_API int dg_block_generate(const dg_head_desc* desc, int32_t n_blocks, const int32_t* y_blocks,
+                             int32_t* y_work, int32_t* canvas, dg_canvas_state* state,
+                             void* h_buffer, const dg_loop_params* params, int32_t n_content,
+                             float s_content, float s_pad, int32_t* tokens_out,
+                             dg_canvas_state* states_out, void* workspace, size_t workspace_bytes,
+                             uint32_t* status, dg_stream_t stream);
 
 /*
  * dg_canvas_step without a caller-supplied workspace, for callers that cannot allocate device

@@ -53,6 +53,8 @@ int main(void) {
   printf("dg_loop_params %zu\n", sizeof(dg_loop_params));
   P(dg_loop_params, keep_sched) P(dg_loop_params, seed) P(dg_loop_params, start_pass)
   P(dg_loop_params, trace_h) P(dg_loop_params, trace_entropy) P(dg_loop_params, trace_timeline)
+  P(dg_loop_params, temp_start) P(dg_loop_params, temp_end) P(dg_loop_params, row_offset)
+  P(dg_stop_rule, keep_rule) P(dg_stop_rule, redraw_mode) P(dg_stop_rule, mask_id)
   printf("dg_synth_params %zu\n", sizeof(dg_synth_params));
   P(dg_synth_params, n_content) P(dg_synth_params, s_pad) P(dg_synth_params, status)
   return 0;
@@ -116,3 +118,26 @@ def test_status_strings(dg):
         s = dg.dg_status_string(code)
         assert s and "unknown" not in s
     assert dg.lib().dg_version() >= 100
+
+
+def test_rule_and_schedule_checks(dg):
+    """Keep / re-draw variants and the temperature schedule are validated before any device
+    work: an unknown keep rule or re-draw mode, a mask id outside [0, V), a negative or
+    one-sided temperature schedule are DG_ERR_INVALID_ARG."""
+    desc = _desc(dg)
+    L = dg.lib()
+    bad = [dg.pass_rule(keep_rule=2), dg.pass_rule(mask_id=4096), dg.pass_rule(mask_id=-1)]
+    bad[2].redraw_mode = dg.REDRAW_MASK
+    r3 = dg.pass_rule()
+    r3.redraw_mode = 5
+    bad.append(r3)
+    for rule in bad:
+        assert L.dg_canvas_step(C.byref(desc), 16, 16, 1, 0, 0, None, None, None, None, None,
+                                None, C.byref(rule), None, 0, None, None) == -1
+    for ts, te in ((-1.0, 0.4), (0.8, 0.0), (0.8, -0.4), (float("nan"), 0.4)):
+        params = dg.LoopParams(rule=dg.pass_rule(), keep_k0=1, temp_start=ts, temp_end=te)
+        params.rule.max_passes = 4
+        params.rule.stable_passes = 2
+        desc_h = _desc(dg, h=8192)
+        assert L.dg_canvas_loop(C.byref(desc_h), 16, 8192, C.byref(params), 16, None, 32, None,
+                                None, None, None, 0, None, None) == -1

@@ -296,3 +296,96 @@ def test_loop_timeline_trace(dg):
         prev_end = m[1]
     for p in range(P, cfg.max_passes):
         assert tl[p]["head"] is None and tl[p]["merge"] is None
+
+
+def _lockstep_rules(dg, orc, res, cfg, x, dtype, *, temp=None, keep_rule=0, mask_id=-1,
+                    row_offset=0):
+    """Per-pass check of a loop run with a temperature schedule / keep rule / masked variant /
+    row offset: the oracle recomputes each pass from the GPU's own canvas and hidden states."""
+    R, S, V, d = cfg.R, cfg.S, cfg.V, cfg.d
+    st = dg.state_fields(res["state"])
+    P = int(st["passes"].max())
+    tc = host(res["trace_canvas"])
+    th = host(res["trace_h"].view(torch.int16)).view(np.uint16)
+    tm = host(res["trace_mean_entropy"])
+    ta, tcf, te = host(res["trace_argmax"]), host(res["trace_conf"]), host(res["trace_entropy"])
+    final = host(res["canvas"])
+    init = (np.full(R, mask_id, np.int32) if mask_id >= 0
+            else orc.draw(cfg.seed, 0xFFFFFFFF, row_offset + np.arange(R, dtype=np.uint64), V))
+    assert np.array_equal(tc[0], init)
+    for p in range(P):
+        c_next = tc[p + 1] if p + 1 < P else final
+        inv_temp = 1.0 if temp is None else 1.0 / orc.temperature(p, cfg.max_passes, *temp)
+        K = min(cfg.keep_k * (p + 1), S)
+        o = orc.step(cfg.B, S, V, d, dtype, th[p].reshape(-1), x["w"], K, cfg.seed, p,
+                     w_scale=x.get("w_scale"), inv_temp=inv_temp, keep_rule=keep_rule,
+                     mask_id=mask_id, row_offset=row_offset)
+        check_stats({"argmax": ta[p], "conf": tcf[p], "entropy": te[p]}, o, TOL[dtype])
+        assert abs(tm[p][0] - o["mean_entropy"][0]) <= TOL[dtype]
+        key = tcf[p].astype(np.float64) if keep_rule == 0 else -te[p].astype(np.float64)
+        kept = _gpu_kept(key, S, K).astype(bool)
+        dropped = (np.full(R, mask_id) if mask_id >= 0 else
+                   orc.draw(cfg.seed, p, row_offset + np.arange(R, dtype=np.uint64), V))
+        assert np.array_equal(c_next, np.where(kept, ta[p], dropped)), f"pass {p}"
+    return P
+
+
+@pytest.mark.parametrize("variant", ["temperature", "entropy_keep", "masked", "row_offset"])
+def test_loop_rule_variants_lockstep(dg, orc, variant):
+    """The NEXT-row sampler variants through the whole loop: the 0.8 -> 0.4 temperature
+    schedule, lowest-entropy keep, the masked variant (start all-mask, re-mask), and a block's
+    re-draw row offset, each checked pass by pass against the oracle."""
+    from workloads import CONFIGS, make_loop_inputs
+    cfg = CONFIGS["loop_bf16_v32768_d256"]
+    x = make_loop_inputs(cfg)
+    kw = {}
+    chk = {}
+    if variant == "temperature":
+        kw = dict(temp_start=0.8, temp_end=0.4)
+        chk = dict(temp=(0.8, 0.4))
+    elif variant == "entropy_keep":
+        kw = chk = dict(keep_rule=1)
+    elif variant == "masked":
+        kw = dict(mask_id=0)
+        chk = dict(mask_id=0)
+    else:
+        kw = chk = dict(row_offset=7 * cfg.R)
+    tw = dev_bf16(x["w"], (cfg.V, cfg.d))
+    canvas = torch.empty(cfg.R, dtype=torch.int32, device="cuda")
+    res = dg.dg_canvas_loop(tw, canvas, B=cfg.B, S=cfg.S, theta=cfg.theta, y=dev(x["y"]),
+                            keep_k0=cfg.keep_k, seed=cfg.seed, max_passes=cfg.max_passes,
+                            stable_passes=cfg.stable_passes, n_content=cfg.n_content,
+                            s_content=cfg.s_content, s_pad=cfg.s_pad, trace=True, **kw)
+    torch.cuda.synchronize()
+    assert int(res["status"][0]) == 0
+    P = _lockstep_rules(dg, orc, res, cfg, x, "bf16", **chk)
+    assert 1 <= P <= cfg.max_passes
+
+
+def test_block_generate(dg, orc):
+    """Block-autoregressive driver: (1) with one pass and nothing kept, the committed tokens of
+    block i are the oracle's draws with rows offset by i*B*S; (2) every block equals a single
+    loop run with that block's targets and row offset (one captured graph serves all blocks)."""
+    from workloads import CONFIGS, make_loop_inputs
+    cfg = CONFIGS["loop_bf16_v32768_d256"]
+    x = make_loop_inputs(cfg)
+    n, R = 3, cfg.R
+    rng = np.random.default_rng(17)
+    yb = np.concatenate([x["y"]] + [np.where(x["y"] > 0, rng.integers(1, cfg.V, R), 0).astype(np.int32)
+                                    for _ in range(n - 1)])
+    tw, tyb = dev_bf16(x["w"], (cfg.V, cfg.d)), dev(yb)
+    base = dict(B=cfg.B, S=cfg.S, theta=cfg.theta, seed=cfg.seed, n_content=cfg.n_content,
+                s_content=cfg.s_content, s_pad=cfg.s_pad)
+    r1 = dg.dg_block_generate(tw, tyb, n_blocks=n, keep_k0=0, max_passes=1, **base)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(r1["tokens"]), orc.draw(cfg.seed, 0, np.arange(n * R), cfg.V))
+    r2 = dg.dg_block_generate(tw, tyb, n_blocks=n, keep_k0=cfg.keep_k, **base)
+    torch.cuda.synchronize()
+    states = host(r2["states"]).reshape(n, cfg.B, 8)
+    for i in range(n):
+        c = torch.empty(R, dtype=torch.int32, device="cuda")
+        one = dg.dg_canvas_loop(tw, c, y=dev(yb[i * R:(i + 1) * R]), keep_k0=cfg.keep_k,
+                                row_offset=i * R, **base)
+        torch.cuda.synchronize()
+        assert torch.equal(c, r2["tokens"][i * R:(i + 1) * R]), f"block {i}"
+        assert int(dg.state_fields(one["state"])["passes"][0]) == states[i, 0, 0]

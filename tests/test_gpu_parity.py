@@ -266,3 +266,30 @@ def test_redraw_modulo_edges(dg, orc, V):
         r = dg.dg_canvas_step(th, tw, canvas, 0, seed, pass_, B=B, S=S)
         torch.cuda.synchronize()
         assert np.array_equal(host(r["canvas"]), orc.draw(seed, pass_, np.arange(B * S), V))
+
+
+@pytest.mark.parametrize("keep_rule,mask", [(1, None), (0, 0), (1, 2999)])
+def test_keep_rule_and_mask_variants(dg, orc, keep_rule, mask):
+    """Lowest-entropy keep and the masked variant (re-mask instead of re-draw) against the
+    oracle: statistics in tolerance, the kept set exact where the oracle's key gap across the
+    keep boundary exceeds 1e-3, dropped slots exactly the mask id or the counter-hash draw."""
+    B, S, V, d, K, seed, p = 2, 200, 3000, 256, 57, 13, 4
+    h, w, canvas = _rand_case(B, S, V, d, 31 + keep_rule, "bf16")
+    hb, wb = _bits(h), _bits(w)
+    res = dg.dg_canvas_step(dev_bf16(hb, (B * S, d)), dev_bf16(wb, (V, d)), dev(canvas), K, seed,
+                            p, B=B, S=S, keep_rule=keep_rule, mask_id=mask)
+    torch.cuda.synchronize()
+    g = {k: host(v) for k, v in res.items() if torch.is_tensor(v)}
+    o = orc.step(B, S, V, d, "bf16", hb, wb, K, seed, p, keep_rule=keep_rule,
+                 mask_id=-1 if mask is None else mask)
+    check_stats(g, o, TOL["bf16"])
+    key_g = g["conf"].astype(np.float64) if keep_rule == 0 else -g["entropy"].astype(np.float64)
+    for b in range(B):
+        sl = slice(b * S, (b + 1) * S)
+        assert g["kept"][sl].sum() == K
+        order = np.lexsort((np.arange(S), -key_g[sl]))
+        assert set(np.nonzero(g["kept"][sl])[0]) == set(order[:K])   # the GPU's own ranking
+        if o["kgap"][b] > 1e-3:
+            assert np.array_equal(g["kept"][sl], o["kept"][sl])
+    dropped = orc.draw(seed, p, np.arange(B * S), V) if mask is None else np.full(B * S, mask)
+    assert np.array_equal(g["canvas"], np.where(g["kept"] == 1, g["argmax"], dropped))

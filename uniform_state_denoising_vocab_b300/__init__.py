@@ -20,13 +20,16 @@ __all__ = ["DG_F32", "DG_BF16", "DG_E4M3", "HeadDesc", "CanvasState", "StopRule"
            "SynthParams", "DgError", "lib", "dg_workspace_bytes", "dg_canvas_stats",
            "dg_canvas_step", "dg_canvas_loop", "dg_status_string", "dtype_code", "new_state",
            "REASON_ENTROPY", "REASON_STABLE", "REASON_CAP", "ST_BAD_TOKEN", "ST_NONFINITE",
-           "ST_TIMEOUT", "STOP_OR", "STOP_AND"]
+           "ST_TIMEOUT", "STOP_OR", "STOP_AND", "KEEP_CONFIDENCE", "KEEP_ENTROPY",
+           "REDRAW_UNIFORM", "REDRAW_MASK", "pass_rule", "dg_block_generate", "timeline_us"]
 
 DG_F32, DG_BF16, DG_E4M3 = 0, 1, 2
 DG_TL_DENOISE, DG_TL_HEAD, DG_TL_MERGE, DG_TL_KERNELS = 0, 1, 2, 3
 REASON_ENTROPY, REASON_STABLE, REASON_CAP = 1, 2, 4
 ST_BAD_TOKEN, ST_NONFINITE, ST_TIMEOUT = 1, 2, 4
 STOP_OR, STOP_AND = 0, 1
+KEEP_CONFIDENCE, KEEP_ENTROPY = 0, 1
+REDRAW_UNIFORM, REDRAW_MASK = 0, 1
 
 _LIB_PATH = Path(__file__).resolve().parent / "libdgcanvas.so"
 _lib = None
@@ -53,7 +56,8 @@ class CanvasState(C.Structure):
 
 class StopRule(C.Structure):
     _fields_ = [("max_passes", C.c_int32), ("entropy_threshold", C.c_float),
-                ("stable_passes", C.c_int32), ("stop_mode", C.c_int32)]
+                ("stable_passes", C.c_int32), ("stop_mode", C.c_int32), ("keep_rule", C.c_int32),
+                ("redraw_mode", C.c_int32), ("mask_id", C.c_int32)]
 
 
 class LoopParams(C.Structure):
@@ -61,7 +65,8 @@ class LoopParams(C.Structure):
                 ("seed", C.c_uint64), ("start_pass", C.c_uint32), ("init_random", C.c_uint32),
                 ("trace_mean_entropy", C.c_void_p), ("trace_canvas", C.c_void_p),
                 ("trace_h", C.c_void_p), ("trace_argmax", C.c_void_p), ("trace_conf", C.c_void_p),
-                ("trace_entropy", C.c_void_p), ("trace_timeline", C.c_void_p)]
+                ("trace_entropy", C.c_void_p), ("trace_timeline", C.c_void_p),
+                ("temp_start", C.c_float), ("temp_end", C.c_float), ("row_offset", C.c_uint64)]
 
 
 class SynthParams(C.Structure):
@@ -91,6 +96,10 @@ def lib():
         L.dg_status_string.argtypes = [C.c_int]
         L.dg_status_string.restype = C.c_char_p
         L.dg_version.restype = C.c_int
+        L.dg_block_generate.argtypes = [C.POINTER(HeadDesc), C.c_int32, vp, vp, vp, vp, vp,
+                                        C.POINTER(LoopParams), C.c_int32, C.c_float, C.c_float,
+                                        vp, vp, vp, sz, vp, vp]
+        L.dg_block_generate.restype = C.c_int
         L.dg_profile_next_head.argtypes = [C.c_void_p, C.c_void_p]
         L.dg_profile_next_head.restype = C.c_int
         for f in ("dg_workspace_bytes", "dg_canvas_stats", "dg_canvas_step", "dg_canvas_loop"):
@@ -195,11 +204,26 @@ def dg_canvas_stats(h, w, *, B: int, S: int, h_scale=None, w_scale=None, inv_tem
     return out
 
 
+def pass_rule(keep_rule: int = KEEP_CONFIDENCE, mask_id: int | None = None,
+              base: StopRule | None = None) -> StopRule:
+    """A rule carrying a pass's keep / re-draw variant (and, from `base`, its stop test)."""
+    r = StopRule(max_passes=1 << 30, entropy_threshold=0.0, stable_passes=1 << 30,
+                 stop_mode=STOP_OR) if base is None else StopRule.from_buffer_copy(base)
+    r.keep_rule = keep_rule
+    r.redraw_mode = REDRAW_UNIFORM if mask_id is None else REDRAW_MASK
+    r.mask_id = 0 if mask_id is None else int(mask_id)
+    return r
+
+
 def dg_canvas_step(h, w, canvas_in, keep_k: int, seed: int, pass_: int, *, B: int, S: int,
                    canvas_out=None, h_scale=None, w_scale=None, inv_temp: float = 1.0,
-                   state=None, rule: StopRule | None = None, outputs: bool = True,
-                   workspace=None, status=None, stream=None) -> dict:
-    """One canvas pass: statistics, keep the top-K by confidence, re-randomise the rest."""
+                   state=None, rule: StopRule | None = None, keep_rule: int = KEEP_CONFIDENCE,
+                   mask_id: int | None = None, outputs: bool = True, workspace=None, status=None,
+                   stream=None) -> dict:
+    """One canvas pass: statistics, keep the top-K by confidence (or the K lowest-entropy slots
+    with keep_rule=KEEP_ENTROPY), re-randomise the rest (or set them to mask_id)."""
+    if rule is None and (keep_rule != KEEP_CONFIDENCE or mask_id is not None):
+        rule = pass_rule(keep_rule, mask_id)
     dev = w.device
     R = B * S
     desc = make_desc(h, w, B=B, S=S, h_scale=h_scale, w_scale=w_scale, inv_temp=inv_temp)
@@ -230,7 +254,9 @@ def dg_canvas_loop(w, canvas, *, B: int, S: int, theta: float, y=None, denoise=N
                    stop_mode: int = STOP_OR, start_pass: int = 0, init_random: bool = True,
                    state=None, n_content: int = 50, s_content: float = 8.0, s_pad: float = 16.0,
                    trace: bool = False, timeline: bool = False, workspace=None, status=None,
-                   outputs: dict | None = None, stream=None) -> dict:
+                   outputs: dict | None = None, keep_rule: int = KEEP_CONFIDENCE,
+                   mask_id: int | None = None, temp_start: float = 0.0, temp_end: float = 0.0,
+                   row_offset: int = 0, stream=None) -> dict:
     """The whole denoising loop on the device (one graph launch, no host synchronisation).
 
     With y given (and denoise None) the built-in synthetic denoiser is used. `denoise`, if
@@ -260,8 +286,10 @@ def dg_canvas_loop(w, canvas, *, B: int, S: int, theta: float, y=None, denoise=N
     for k in ("conf", "entropy"):
         if out[k] is None:
             out[k] = torch.empty(R, dtype=torch.float32, device=dev)
-    params = LoopParams(rule=StopRule(max_passes=max_passes, entropy_threshold=theta,
-                                      stable_passes=stable_passes, stop_mode=stop_mode),
+    params = LoopParams(rule=pass_rule(keep_rule, mask_id,
+                                       StopRule(max_passes=max_passes, entropy_threshold=theta,
+                                                stable_passes=stable_passes, stop_mode=stop_mode)),
+                        temp_start=temp_start, temp_end=temp_end, row_offset=row_offset,
                         keep_k0=keep_k0, keep_sched=None if keep_sched is None else _ptr(keep_sched).value,
                         seed=seed, start_pass=start_pass, init_random=1 if init_random else 0)
     if trace:
@@ -300,6 +328,41 @@ def dg_canvas_loop(w, canvas, *, B: int, S: int, theta: float, y=None, denoise=N
                           _ptr(out["entropy"]), _ptr(ws), ws.numel(), _ptr(st), _stream(stream))
     _check(rc, "dg_canvas_loop")
     out["_keepalive"] = keep + [ws, desc, params]
+    return out
+
+
+def dg_block_generate(w, y_blocks, *, n_blocks: int, B: int, S: int, theta: float,
+                      w_scale=None, keep_k0: int = 32, seed: int = 0, max_passes: int = 48,
+                      stable_passes: int = 2, stop_mode: int = STOP_OR, n_content: int = 50,
+                      s_content: float = 8.0, s_pad: float = 16.0, keep_rule: int = KEEP_CONFIDENCE,
+                      mask_id: int | None = None, temp_start: float = 0.0, temp_end: float = 0.0,
+                      row_offset: int = 0, workspace=None, status=None, stream=None) -> dict:
+    """Block-autoregressive generation with the built-in synthetic denoiser: n_blocks loops, one
+    per block of B*S slots with targets y_blocks[i], each committing its final canvas."""
+    dev = w.device
+    R = B * S
+    d = int(w.shape[1])
+    h_buffer = torch.empty(R, d, dtype=torch.bfloat16, device=dev)
+    desc = make_desc(h_buffer, w, B=B, S=S, w_scale=w_scale)
+    ws = _workspace(desc, dev, workspace)
+    st = torch.zeros(1, dtype=torch.int32, device=dev) if status is None else status
+    out = {"tokens": torch.empty(n_blocks * R, dtype=torch.int32, device=dev),
+           "states": torch.zeros(n_blocks * B, 8, dtype=torch.int32, device=dev), "status": st}
+    y_work = torch.empty(R, dtype=torch.int32, device=dev)
+    canvas = torch.empty(R, dtype=torch.int32, device=dev)
+    state = new_state(B, dev)
+    params = LoopParams(rule=pass_rule(keep_rule, mask_id,
+                                       StopRule(max_passes=max_passes, entropy_threshold=theta,
+                                                stable_passes=stable_passes, stop_mode=stop_mode)),
+                        keep_k0=keep_k0, seed=seed, temp_start=temp_start, temp_end=temp_end,
+                        row_offset=row_offset)
+    rc = lib().dg_block_generate(C.byref(desc), int(n_blocks), _ptr(y_blocks), _ptr(y_work),
+                                 _ptr(canvas), _ptr(state), _ptr(h_buffer), C.byref(params),
+                                 int(n_content), float(s_content), float(s_pad),
+                                 _ptr(out["tokens"]), _ptr(out["states"]), _ptr(ws), ws.numel(),
+                                 _ptr(st), _stream(stream))
+    _check(rc, "dg_block_generate")
+    out["_keepalive"] = [ws, desc, params, y_work, canvas, state, h_buffer]
     return out
 
 

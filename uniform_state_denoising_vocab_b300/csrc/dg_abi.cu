@@ -161,8 +161,10 @@ struct Prepared {
     DeviceInfo di;
     Layout L;
     unsigned long long* timeline = nullptr;  // loop timeline (head stamps) or null
-    const int32_t* tl_pass = nullptr;
+    const int32_t* pass_ptr = nullptr;       // loop pass index (device) or null
     const int32_t* stop = nullptr;           // loop stop flag (device) or null
+    float temp_start = 0.f, temp_end = 0.f;  // loop temperature schedule
+    int temp_passes = 0;                     // its max_passes, 0 = none
 };
 
 int prepare(const dg_head_desc* d, void* ws, size_t ws_bytes, Prepared* P, bool need_h = true) {
@@ -227,8 +229,11 @@ cudaError_t launch_head_only(const dg_head_desc* d, const Prepared& P, uint8_t* 
     a.partials = reinterpret_cast<float4*>(ws + P.L.off_partials);
     a.status = status;
     a.timeline = P.timeline;
-    a.tl_pass = P.tl_pass;
+    a.pass_ptr = P.pass_ptr;
     a.stop = P.stop;
+    a.temp_start = P.temp_start;
+    a.temp_end = P.temp_end;
+    a.temp_passes = P.temp_passes;
     a.w_scale = d->w_scale;
     a.h_scale = d->h_scale;
     cudaError_t e = cudaSuccess;
@@ -272,6 +277,21 @@ SelectArgs base_select(const dg_head_desc* d, const Prepared& P, uint8_t* ws, ui
     s.inv_v = 1.0 / static_cast<double>(d->V);
     s.status = status;
     return s;
+}
+
+// Checks the keep / re-draw part of a rule against the vocabulary size.
+bool rule_ok(const dg_stop_rule& r, int V) {
+    if (r.keep_rule != DG_KEEP_CONFIDENCE && r.keep_rule != DG_KEEP_ENTROPY) return false;
+    if (r.redraw_mode != DG_REDRAW_UNIFORM && r.redraw_mode != DG_REDRAW_MASK) return false;
+    if (r.redraw_mode == DG_REDRAW_MASK && (r.mask_id < 0 || r.mask_id >= V)) return false;
+    return true;
+}
+
+void set_rule(SelectArgs* s, const dg_stop_rule& r) {
+    s->rule = r;
+    s->keep_rule = r.keep_rule;
+    s->redraw_mode = r.redraw_mode;
+    s->mask_id = r.mask_id;
 }
 
 // Point the per-row statistics at the caller's arrays, or at workspace scratch where NULL.
@@ -354,6 +374,7 @@ int dg_canvas_step(const dg_head_desc* desc, const int32_t* canvas_in, int32_t* 
     if (rule && (rule->max_passes < 1 || rule->stable_passes < 1 ||
                  (rule->stop_mode != DG_STOP_OR && rule->stop_mode != DG_STOP_AND)))
         return DG_ERR_INVALID_ARG;
+    if (rule && (!desc || !rule_ok(*rule, desc->V))) return DG_ERR_INVALID_ARG;
     Prepared P;
     int rc = prepare(desc, workspace, workspace_bytes, &P);
     if (rc != DG_OK) return rc;
@@ -371,7 +392,7 @@ int dg_canvas_step(const dg_head_desc* desc, const int32_t* canvas_in, int32_t* 
     s.pass = pass;
     s.state = state;
     if (rule) {
-        s.rule = *rule;
+        set_rule(&s, *rule);
         s.has_rule = 1;
     }
     if (launch_select(s, st) != cudaSuccess) return DG_ERR_CUDA;
@@ -461,8 +482,13 @@ void copy_params(dg_loop_params* dst, const dg_loop_params& s) {
     dst->keep_k0 = s.keep_k0;
     dst->keep_sched = s.keep_sched;
     dst->seed = s.seed;
-    dst->start_pass = s.start_pass;
-    dst->init_random = s.init_random;
+    // start_pass, init_random and row_offset only feed the loop's set-up kernel, not the graph:
+    // they stay zero in the key so that one graph serves every start
+    dst->rule.keep_rule = s.rule.keep_rule;
+    dst->rule.redraw_mode = s.rule.redraw_mode;
+    dst->rule.mask_id = s.rule.mask_id;
+    dst->temp_start = s.temp_start;
+    dst->temp_end = s.temp_end;
     dst->trace_mean_entropy = s.trace_mean_entropy;
     dst->trace_canvas = s.trace_canvas;
     dst->trace_h = s.trace_h;
@@ -536,8 +562,13 @@ int build_loop_graph(LoopEntry* E, const Prepared& P) {
     const int passes_per_iter = builtin ? 2 : 1;
     Prepared Ph = P;
     Ph.timeline = k.params.trace_timeline;
-    Ph.tl_pass = &ctl->pass;
+    Ph.pass_ptr = &ctl->pass;
     Ph.stop = &ctl->stop;
+    if (k.params.temp_start > 0.f) {
+        Ph.temp_start = k.params.temp_start;
+        Ph.temp_end = k.params.temp_end;
+        Ph.temp_passes = k.params.rule.max_passes;
+    }
     if (fuse_quant) Ph.path = -PATH_TC_E4M3_QUANT;  // quantisation done by the denoiser
     const size_t hbytes = static_cast<size_t>(d->B) * d->S * d->d * elem_size(d->h_dtype);
     for (int it = 0; it < passes_per_iter && rc == DG_OK; ++it) {
@@ -567,7 +598,7 @@ int build_loop_graph(LoopEntry* E, const Prepared& P) {
             s.keep_sched = k.params.keep_sched;
             s.seed = k.params.seed;
             s.state = k.state;
-            s.rule = k.params.rule;
+            set_rule(&s, k.params.rule);
             s.has_rule = 1;
             s.ctl = ctl;
             s.cond = handle;
@@ -624,6 +655,11 @@ extern "C" int dg_canvas_loop(const dg_head_desc* desc, int32_t* canvas, void* h
         return DG_ERR_INVALID_ARG;
     if (params->keep_k0 < 0 || static_cast<int64_t>(params->start_pass) >= r.max_passes)
         return DG_ERR_INVALID_ARG;
+    if (!rule_ok(r, desc->V)) return DG_ERR_INVALID_ARG;
+    if (!(params->temp_start >= 0.f && params->temp_start < 3.0e38f) ||
+        (params->temp_start > 0.f && !(params->temp_end > 0.f && params->temp_end < 3.0e38f)))
+        return DG_ERR_INVALID_ARG;
+
     if (!aligned16(h_buffer) || !aligned16(canvas)) return DG_ERR_ALIGNMENT;
     Prepared P;
     int rc = prepare(desc, workspace, workspace_bytes, &P);
@@ -687,8 +723,10 @@ extern "C" int dg_canvas_loop(const dg_head_desc* desc, int32_t* canvas, void* h
     }
     E->stamp = ++g_stamp;
     const int R = desc->B * desc->S;
-    if (launch_loop_init(canvas, R, desc->S, desc->B, desc->V, params->seed, params->init_random ? 1 : 0,
-                         state, params->start_pass > 0 ? 1 : 0, ctl,
+    const int init_mode =
+        params->init_random ? (r.redraw_mode == DG_REDRAW_MASK ? 2 : 1) : 0;
+    if (launch_loop_init(canvas, R, desc->S, desc->B, desc->V, params->seed, init_mode, r.mask_id,
+                         params->row_offset, state, params->start_pass > 0 ? 1 : 0, ctl,
                          static_cast<int>(params->start_pass), r.max_passes, status,
                          params->trace_timeline, st) != cudaSuccess)
         return DG_ERR_CUDA;
@@ -699,5 +737,49 @@ extern "C" int dg_canvas_loop(const dg_head_desc* desc, int32_t* canvas, void* h
         E->stamp = 0;
     }
     evict_finished_locked();
+    return DG_OK;
+}
+
+extern "C" int dg_block_generate(const dg_head_desc* desc, int32_t n_blocks,
+                                 const int32_t* y_blocks, int32_t* y_work, int32_t* canvas,
+                                 dg_canvas_state* state, void* h_buffer,
+                                 const dg_loop_params* params, int32_t n_content, float s_content,
+                                 float s_pad, int32_t* tokens_out, dg_canvas_state* states_out,
+                                 void* workspace, size_t workspace_bytes, uint32_t* status,
+                                 dg_stream_t stream) {
+    if (!desc || n_blocks < 0 || !y_blocks || !y_work || !canvas || !state || !h_buffer ||
+        !params || !tokens_out || !states_out || desc->B < 1 || desc->S < 1)
+        return DG_ERR_INVALID_ARG;
+    const size_t R = static_cast<size_t>(desc->B) * desc->S;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    dg_synth_params sp;
+    std::memset(&sp, 0, sizeof(sp));
+    sp.desc = desc;
+    sp.y = y_work;
+    sp.n_content = n_content;
+    sp.s_content = s_content;
+    sp.s_pad = s_pad;
+    sp.status = status;
+    dg_loop_params p = *params;
+    p.init_random = 1;
+    p.start_pass = 0;
+    for (int32_t i = 0; i < n_blocks; ++i) {
+        // block i's targets into the work buffer the captured loop reads (one graph for all)
+        if (cudaMemcpyAsync(y_work, y_blocks + i * R, R * sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                            st) != cudaSuccess)
+            return DG_ERR_CUDA;
+        p.row_offset = params->row_offset + static_cast<uint64_t>(i) * R;
+        const int rc = dg_canvas_loop(desc, canvas, h_buffer, &p, dg_synth_denoise, &sp, state,
+                                      nullptr, nullptr, nullptr, workspace, workspace_bytes, status,
+                                      stream);
+        if (rc != DG_OK) return rc;
+        // commit the block's final canvas and its per-canvas loop state
+        if (cudaMemcpyAsync(tokens_out + i * R, canvas, R * sizeof(int32_t),
+                            cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
+            cudaMemcpyAsync(states_out + static_cast<size_t>(i) * desc->B, state,
+                            static_cast<size_t>(desc->B) * sizeof(dg_canvas_state),
+                            cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+            return DG_ERR_CUDA;
+    }
     return DG_OK;
 }

@@ -23,14 +23,15 @@ __global__ void __launch_bounds__(BM)
     const int t = threadIdx.x;
     grid_dependency_wait();
     const int units = (args.stop != nullptr && *args.stop != 0) ? 0 : args.MB * args.n_groups;
-    const int tl_pass = args.timeline != nullptr ? *args.tl_pass : 0;
+    const int tl_pass = args.timeline != nullptr ? *args.pass_ptr : 0;
+    const float crow_base = pass_crow_base(args);
     if (units > 0) timeline_begin(args.timeline, tl_pass, DG_TL_HEAD);
     grid_launch_dependents();
     for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
         const int mb = unit % args.MB, grp = unit / args.MB;
         const int row = mb * BM + t;
         const bool row_ok = row < args.R;
-        const float crow = args.crow_base;
+        const float crow = crow_base;
         RowState st = row_state_init();
         for (int nb = grp; nb < args.NT; nb += args.n_groups) {
             float acc[BN];

@@ -110,7 +110,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     grid_dependency_wait();  // the prologue above overlaps the previous kernel of the stream
     // a pass after the loop has ended (second pass of a graph iteration) does no work
     const int units = (args.stop != nullptr && *args.stop != 0) ? 0 : args.MB * args.n_groups;
-    const int tl_pass = args.timeline != nullptr ? *args.tl_pass : 0;
+    const int tl_pass = args.timeline != nullptr ? *args.pass_ptr : 0;
+    const float crow_base = pass_crow_base(args);
     if (units > 0) timeline_begin(args.timeline, tl_pass, DG_TL_HEAD);
     grid_launch_dependents();
 
@@ -211,7 +212,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int unit = pair; unit < units && ok; unit += n_pairs) {
             const int mb = unit % args.MB, grp = unit / args.MB;
             const int row = mb * (2 * BM) + static_cast<int>(rank) * BM + row_in_cta;
-            float crow = args.crow_base;
+            float crow = crow_base;
             if (KIND == 1 && args.h_scale != nullptr && row < args.R) crow *= args.h_scale[row];
             RowState st = row_state_init();
             for (int nb = grp; nb < args.NT && ok; nb += args.n_groups, ++tcount) {

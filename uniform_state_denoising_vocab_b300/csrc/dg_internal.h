@@ -44,9 +44,23 @@ struct HeadArgs {
     float4* partials;         // [R][n_groups]: the partials of one row are contiguous
     uint32_t* status;         // sticky status word or null
     unsigned long long* timeline;  // loop timeline (dg_loop_params.trace_timeline) or null
-    const int32_t* tl_pass;        // pass index for the timeline (device)
+    const int32_t* pass_ptr;       // loop mode: the pass index (device), else null
     const int32_t* stop;           // loop mode: non-zero = the loop has ended, do nothing
+    float temp_start, temp_end;    // loop temperature schedule (temp_passes > 0)
+    int temp_passes;               // max_passes of the schedule, 0 = none
 };
+
+// The logit scale of a pass, in base-2 units: crow_base (= inv_temp * log2 e), divided by the
+// pass's temperature T_p = t0 + (t1 - t0) * p / (P - 1) when a schedule is set (fp32).
+__device__ __forceinline__ float pass_crow_base(const HeadArgs& a) {
+    if (a.temp_passes <= 0 || a.pass_ptr == nullptr) return a.crow_base;
+    const int p = *a.pass_ptr;
+    const float T = a.temp_passes > 1
+                        ? a.temp_start + __fdiv_rn((a.temp_end - a.temp_start) * static_cast<float>(p),
+                                                   static_cast<float>(a.temp_passes - 1))
+                        : a.temp_start;
+    return __fdiv_rn(a.crow_base, T);
+}
 
 // Programmatic dependent launch. Every kernel of a pass is launched with the programmatic
 // stream-serialization attribute, so it may be scheduled while its predecessor in the stream is
@@ -98,6 +112,7 @@ struct LoopCtl {
     uint32_t ticket;    // canvases of the merge kernel finished in this pass
     int32_t max_passes;
     int32_t stop;       // set once the loop has ended: later passes of a graph iteration are no-ops
+    uint64_t row_offset;  // added to the row index of every re-draw key
 };
 
 struct SelectArgs {
@@ -111,6 +126,9 @@ struct SelectArgs {
     const int32_t* canvas_in;         // null: statistics only
     int32_t* canvas_out;
     double inv_v;                     // RN(1 / V) for the exact draw modulo
+    int keep_rule;                    // DG_KEEP_CONFIDENCE / DG_KEEP_ENTROPY
+    int redraw_mode;                  // DG_REDRAW_UNIFORM / DG_REDRAW_MASK
+    int mask_id;
     int keep_k;                       // fixed K when keep_k0 < 0
     int keep_k0;                      // >= 0: K_t = min(keep_k0 * (p + 1), S)
     const int32_t* keep_sched;        // optional [max_passes]
@@ -138,9 +156,11 @@ cudaError_t launch_quant_rows(const uint16_t* h, int R, int d, uint8_t* q, float
                               uint32_t* status, cudaStream_t stream);
 
 // Loop set-up: optional random initial canvas, state reset, control block reset.
+// init_random: 1 = uniform draws key(seed, 0xFFFFFFFF, row_offset + r) mod V, 2 = mask_id.
 cudaError_t launch_loop_init(int32_t* canvas, int R, int S, int B, int V, uint64_t seed,
-                             int init_random, dg_canvas_state* state, int keep_stable,
-                             LoopCtl* ctl, int start_pass, int max_passes, uint32_t* status,
+                             int init_random, int mask_id, uint64_t row_offset,
+                             dg_canvas_state* state, int keep_stable, LoopCtl* ctl,
+                             int start_pass, int max_passes, uint32_t* status,
                              unsigned long long* timeline, cudaStream_t stream);
 
 // Copy rows of one pass into a trace buffer at offset pass * bytes (pass read on device).

@@ -53,12 +53,13 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v
 }
 
 struct MergeSmem {
-    float conf[kMaxRowsPerCta];      // this CTA's rows: confidence, entropy, argmax
+    float key[kMaxRowsPerCta];       // this CTA's rows: keep key (larger = kept first),
+    float conf[kMaxRowsPerCta];      // confidence, entropy, argmax
     float ent[kMaxRowsPerCta];
     int32_t arg[kMaxRowsPerCta];
     int32_t old[kMaxRowsPerCta];     // this CTA's slots' tokens before the pass
     int32_t draw[kMaxRowsPerCta];    // this CTA's slots' re-randomised tokens for the pass
-    float all_conf[1024];            // every slot of the canvas (gathered over the cluster)
+    float all_key[1024];             // every slot's keep key (gathered over the cluster)
     float warp_ent[32];              // CTA 0: per-warp sums of the entropy tree
     uint32_t changed[kMergeCluster]; // CTA 0: per-CTA "some slot changed" flags (pushed)
 };
@@ -69,8 +70,8 @@ struct MergeSmem {
 // then the lanes combine with a fixed xor butterfly (lower lane first), so every run merges in
 // the same order and all lanes end with the same result. After a cluster barrier every CTA reads
 // the whole canvas's confidences from the cluster's shared memory and ranks its own slots by
-// (confidence desc, slot asc): kept <=> rank < K; kept slots take their argmax, the others the
-// counter-hash draw. CTA 0 forms the mean entropy (fixed-order pairwise tree over the slots) and,
+// (key desc, slot asc), the key being the confidence or the negated entropy: kept <=> rank < K;
+// kept slots take their argmax, the others the counter-hash draw (or the mask token). CTA 0 forms the mean entropy (fixed-order pairwise tree over the slots) and,
 // after a second barrier, applies the stop rules; in loop mode the last canvas of the pass
 // advances the pass and sets the graph condition.
 __global__ void __cluster_dims__(kMergeCluster, 1, 1) __maxnreg__(40)
@@ -92,6 +93,7 @@ __global__ void __cluster_dims__(kMergeCluster, 1, 1) __maxnreg__(40)
     // Loads that do not depend on whether the canvas is frozen go out first: its state word,
     // the old tokens of this CTA's slots and the partials of each warp's rows.
     const int done = a.state != nullptr ? __ldcg(&a.state[b].done) : 0;  // same in every CTA of b
+    const uint64_t row_off = a.ctl != nullptr ? __ldcg(&a.ctl->row_offset) : 0ull;
     int old_tok = 0;
     if (a.canvas_out && tid < nrows) old_tok = __ldcg(a.canvas_in + base + j0 + tid);
     // CTA 0 applies the stop rule: its inputs are fetched now
@@ -120,9 +122,12 @@ __global__ void __cluster_dims__(kMergeCluster, 1, 1) __maxnreg__(40)
                 v[i] = g < a.n_groups ? __ldcg(q + g) : pack(partial_empty());
             }
             if (g0 == 0 && lane == 0 && a.canvas_out)  // integer work while the loads fly
-                sm.draw[jj] = static_cast<int32_t>(mod_u64_by_u32(
-                    draw_key(a.seed, static_cast<uint32_t>(p), static_cast<uint64_t>(r)),
-                    static_cast<uint32_t>(a.V), a.inv_v));
+                sm.draw[jj] = a.redraw_mode == DG_REDRAW_MASK
+                                  ? a.mask_id
+                                  : static_cast<int32_t>(mod_u64_by_u32(
+                                        draw_key(a.seed, static_cast<uint32_t>(p),
+                                                 row_off + static_cast<uint64_t>(r)),
+                                        static_cast<uint32_t>(a.V), a.inv_v));
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc = partial_merge(acc, unpack(v[i]));
         }
@@ -135,6 +140,7 @@ __global__ void __cluster_dims__(kMergeCluster, 1, 1) __maxnreg__(40)
             const float s = acc.s;
             sm.conf[jj] = 1.0f / s;
             sm.ent[jj] = fmaxf(kLn2 * (log2f(s) - acc.u / s), 0.0f);
+            sm.key[jj] = a.keep_rule == DG_KEEP_ENTROPY ? -sm.ent[jj] : sm.conf[jj];
             sm.arg[jj] = acc.idx;
             if (!(isfinite(s) && isfinite(acc.u) && isfinite(acc.mx) && s >= 1.0f - 1e-3f))
                 flag_status(a.status, DG_ST_NONFINITE);
@@ -160,14 +166,14 @@ __global__ void __cluster_dims__(kMergeCluster, 1, 1) __maxnreg__(40)
             }
         }
 
-        // gather the canvas's confidences from the cluster; CTA 0 also sums the entropies with a
+        // gather the canvas's keep keys from the cluster; CTA 0 also sums the entropies with a
         // fixed-order tree: pairwise within each warp of 32 consecutive slots (xor butterfly),
         // then the per-warp sums in increasing order
         float ent_i = 0.0f;
         for (int i = tid; i < S; i += kMergeThreads) {
             const uint32_t owner = static_cast<uint32_t>(i / rpc);
             const int off = i - static_cast<int>(owner) * rpc;
-            sm.all_conf[i] = ld_cluster_f32(mapa_shared(smem_u32(&sm.conf[off]), owner));
+            sm.all_key[i] = ld_cluster_f32(mapa_shared(smem_u32(&sm.key[off]), owner));
             if (c == 0) ent_i = ld_cluster_f32(mapa_shared(smem_u32(&sm.ent[off]), owner));
         }
         if (c == 0) {
@@ -196,9 +202,9 @@ __global__ void __cluster_dims__(kMergeCluster, 1, 1) __maxnreg__(40)
             const bool act = jj < nrows;
             const int j = j0 + jj;
             if (act) {
-                const float cj = sm.all_conf[j];
+                const float cj = sm.all_key[j];
                 for (int i = sub; i < S; i += tpr) {
-                    const float ci = sm.all_conf[i];
+                    const float ci = sm.all_key[i];
                     rank += (ci > cj) || (ci == cj && i < j);
                 }
             }
@@ -338,9 +344,9 @@ __global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ h, int d, ui
 }
 
 __global__ void loop_init_kernel(int32_t* canvas, int S, int V, uint64_t seed, int init_random,
-                                 dg_canvas_state* state, int keep_stable, LoopCtl* ctl,
-                                 int start_pass, int max_passes, uint32_t* status,
-                                 unsigned long long* timeline) {
+                                 int mask_id, uint64_t row_offset, dg_canvas_state* state,
+                                 int keep_stable, LoopCtl* ctl, int start_pass, int max_passes,
+                                 uint32_t* status, unsigned long long* timeline) {
     const int b = blockIdx.x;
     if (timeline)
         for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < max_passes * DG_TL_KERNELS;
@@ -350,9 +356,12 @@ __global__ void loop_init_kernel(int32_t* canvas, int S, int V, uint64_t seed, i
         }
     for (int j = threadIdx.x; j < S; j += blockDim.x) {
         const int r = b * S + j;
-        if (init_random) {
-            canvas[r] = static_cast<int32_t>(draw_key(seed, kInitPass, static_cast<uint64_t>(r)) %
-                                             static_cast<uint64_t>(V));
+        if (init_random == 2) {
+            canvas[r] = mask_id;
+        } else if (init_random) {
+            canvas[r] = static_cast<int32_t>(
+                draw_key(seed, kInitPass, row_offset + static_cast<uint64_t>(r)) %
+                static_cast<uint64_t>(V));
         } else {
             const int c = canvas[r];
             if (c < 0 || c >= V) flag_status(status, DG_ST_BAD_TOKEN);
@@ -373,6 +382,7 @@ __global__ void loop_init_kernel(int32_t* canvas, int S, int V, uint64_t seed, i
             ctl->ticket = 0;
             ctl->max_passes = max_passes;
             ctl->stop = 0;
+            ctl->row_offset = row_offset;
         }
     }
 }
@@ -668,12 +678,14 @@ cudaError_t launch_quant_rows(const uint16_t* h, int R, int d, uint8_t* q, float
 }
 
 cudaError_t launch_loop_init(int32_t* canvas, int R, int S, int B, int V, uint64_t seed,
-                             int init_random, dg_canvas_state* state, int keep_stable, LoopCtl* ctl,
+                             int init_random, int mask_id, uint64_t row_offset,
+                             dg_canvas_state* state, int keep_stable, LoopCtl* ctl,
                              int start_pass, int max_passes, uint32_t* status,
                              unsigned long long* timeline, cudaStream_t stream) {
     (void)R;
-    loop_init_kernel<<<B, 256, 0, stream>>>(canvas, S, V, seed, init_random, state, keep_stable, ctl,
-                                            start_pass, max_passes, status, timeline);
+    loop_init_kernel<<<B, 256, 0, stream>>>(canvas, S, V, seed, init_random, mask_id, row_offset,
+                                            state, keep_stable, ctl, start_pass, max_passes,
+                                            status, timeline);
     return cudaGetLastError();
 }
 
