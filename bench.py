@@ -147,6 +147,24 @@ def load_peaks():
 
 DATASHEET = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0, "e4m3_tflops": 4500.0}
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the head kernel,
+# from an ncu capture of the build whose head sources hash to `src` (summaries in profiles/).
+# A different hash means the kernel changed since the counters were taken: traffic is null.
+HEAD_SOURCES = ["dg_head_tc2.cu", "dg_head_epi.cuh", "dg_common.cuh", "dg_ptx.cuh", "dg_internal.h"]
+TRAFFIC = {
+    "pass_bf16_v262144_d2816": {"bytes": 1.477923e9 + 3.30496e6, "src": "089d8a0aad9fefb0"},
+    "loop_e4m3_v262144_d2816": {"bytes": 740.054784e6 + 2.882816e6, "src": "089d8a0aad9fefb0"},
+}
+
+
+def head_source_hash() -> str:
+    import hashlib
+    hsh = hashlib.sha256()
+    for f in HEAD_SOURCES:
+        with open(os.path.join(ROOT, "uniform_state_denoising_vocab_b300", "csrc", f), "rb") as fh:
+            hsh.update(fh.read())
+    return hsh.hexdigest()[:16]
+
 
 def roofline(cfg, r, peaks, peak_kind, step_s):
     """Roofline of the head kernel (the dominant kernel): t_roof = max(FLOPs / tensor peak,
@@ -169,7 +187,8 @@ def roofline(cfg, r, peaks, peak_kind, step_s):
         achieved = r["flops"] / head_s / 1e12
         out.update(bound="tensor", achieved=achieved, peak=tens, unit="TFLOP/s", frac=achieved / tens,
                    peak_source=f"{peak_kind} sustained bf16 cuBLAS" + (" x2 nominal fp8/bf16" if fp8 else ""))
-    out["traffic"] = None
+    rec = TRAFFIC.get(cfg.name)
+    out["traffic"] = rec["bytes"] if rec and rec["src"] == head_source_hash() else None
     out["kernel"] = {"f32": "head_simt_kernel", "bf16": "head_tc2_kernel<0>",
                      "e4m3": "head_tc2_kernel<1>"}[cfg.precision] if cfg.R > 128 or cfg.precision == "f32" \
         else {"bf16": "head_tc_kernel<0>", "e4m3": "head_tc_kernel<1>"}[cfg.precision]
