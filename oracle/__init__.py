@@ -8,11 +8,15 @@ from .oracle import (  # noqa: F401
     OR_BF16,
     OR_E4M3,
     OR_F32,
+    OR_NVFP4,
     bf16_round,
     build,
     draw,
     e4m3_round,
     e4m3_value,
+    e2m1_round,
+    e2m1_value,
+    quant_rows_nvfp4,
     head_stats,
     keys,
     loop,

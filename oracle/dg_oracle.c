@@ -40,6 +40,7 @@
 #define OR_F32 0
 #define OR_BF16 1
 #define OR_E4M3 2
+#define OR_NVFP4 3
 
 /* ------------------------------------------------------------------------------------------
  * Number formats.
@@ -138,13 +139,99 @@ void or_quant_rows_e4m3(const uint16_t* h, int64_t rows, int64_t d, uint8_t* q, 
     }
 }
 
+/* FP4 E2M1 (OCP Microscaling Formats specification, "FP4 (E2M1)"): 1 sign bit, 2 exponent bits
+ * with bias 1, 1 mantissa bit; exponent field 0 holds the subnormal 0.5 * m; no infinities or
+ * NaN. Magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double or_e2m1_value(uint8_t q) {
+    int sign = (q >> 3) & 1;
+    int e = (q >> 1) & 3;
+    int m = q & 1;
+    double v = (e == 0) ? 0.5 * m : ldexp(1.0 + m / 2.0, e - 1);
+    return sign ? -v : v;
+}
+
+/* Round a binary32 to E2M1, nearest-even, saturating to +-6; NaN is not representable and maps
+ * to +6 here (the quantiser never produces it from finite input). */
+uint8_t or_e2m1_round_satfinite(float xf) {
+    double x = (double)xf;
+    uint8_t s = (!isnan(x) && signbit(x)) ? 0x8 : 0x0;
+    double a = fabs(x);
+    if (isnan(a) || isinf(a)) return s | 0x7;
+    double r = round_sig(a, 2, -1);             /* 2 significant bits, spacing >= 0.5 */
+    if (r > 6.0) r = 6.0;
+    if (r == 0.0) return s;
+    if (r < 1.0) return s | 0x1;                /* the subnormal 0.5 */
+    int e;
+    double f = frexp(r, &e);                    /* r = f * 2^e, leading bit 2^(e-1) */
+    int E = e - 1 + 1;
+    int m = (int)((2.0 * f - 1.0) * 2.0);       /* exact: 1 fraction bit */
+    return s | (uint8_t)(E << 1) | (uint8_t)m;
+}
+
+/* NVFP4 quantisation of bf16 rows (two-level scaling), in IEEE binary32 as stated:
+ *   amax = max_k |h_k|; if amax == 0: row scale g = 1, every block scale and code 0.
+ *   g = fp32(amax / 2688)                                   (2688 = 448 * 6)
+ *   per block of 16 consecutive elements: bmax = max |h_k| over the block,
+ *     sb = e4m3_rn_satfinite(fp32(bmax / fp32(6 * g)))      (the block scale, E4M3 >= 0)
+ *     if sb == 0 every code of the block is 0, else with db = fp32(value(sb) * g):
+ *     q_k = e2m1_rn_satfinite(fp32(h_k / db)).
+ * The element value is e2m1(q_k) * value(sb) * g. Codes are packed two per byte, element 2j in the
+ * low nibble of byte j and element 2j+1 in the high nibble. d must be a multiple of 16. */
+void or_quant_rows_nvfp4(const uint16_t* h, int64_t rows, int64_t d, uint8_t* q, uint8_t* bscale,
+                         float* scale) {
+    const int64_t nb = d / 16;
+    for (int64_t r = 0; r < rows; r++) {
+        float amax = 0.0f;
+        for (int64_t k = 0; k < d; k++) {
+            float a = fabsf((float)or_bf16_value(h[r * d + k]));
+            if (a > amax) amax = a;
+        }
+        uint8_t* qr = q + r * (d / 2);
+        memset(qr, 0, (size_t)(d / 2));
+        if (amax == 0.0f) {
+            scale[r] = 1.0f;
+            memset(bscale + r * nb, 0, (size_t)nb);
+            continue;
+        }
+        volatile float g = amax / 2688.0f;
+        volatile float g6 = 6.0f * g;
+        scale[r] = g;
+        for (int64_t b = 0; b < nb; b++) {
+            float bmax = 0.0f;
+            for (int64_t k = b * 16; k < b * 16 + 16; k++) {
+                float a = fabsf((float)or_bf16_value(h[r * d + k]));
+                if (a > bmax) bmax = a;
+            }
+            volatile float t = bmax / g6;
+            uint8_t sb = or_e4m3_round_satfinite(t);
+            bscale[r * nb + b] = sb;
+            double sv = or_e4m3_value(sb);
+            if (sv == 0.0) continue;
+            volatile float db = (float)sv * g;
+            for (int64_t k = b * 16; k < b * 16 + 16; k++) {
+                volatile float x = (float)or_bf16_value(h[r * d + k]) / db;
+                uint8_t c = or_e2m1_round_satfinite(x);
+                qr[k / 2] |= (uint8_t)(c << (4 * (k & 1)));
+            }
+        }
+    }
+}
+
 /* Widen one stored operand element to double. */
 static inline double operand(int dtype, const void* base, int64_t i) {
     switch (dtype) {
     case OR_F32: return (double)((const float*)base)[i];
     case OR_BF16: return or_bf16_value(((const uint16_t*)base)[i]);
+    case OR_NVFP4: return or_e2m1_value((((const uint8_t*)base)[i / 2] >> (4 * (i & 1))) & 0xF);
     default: return or_e4m3_value(((const uint8_t*)base)[i]);
     }
+}
+
+/* Block scale of element k of a row (NVFP4 operands): value of the E4M3 scale of its block of
+ * 16; 1 for the other formats. */
+static inline double block_scale(int dtype, const uint8_t* bscale, int64_t row, int64_t d,
+                                 int64_t k) {
+    return dtype == OR_NVFP4 ? or_e4m3_value(bscale[row * (d / 16) + k / 16]) : 1.0;
 }
 
 /* ------------------------------------------------------------------------------------------
@@ -164,9 +251,12 @@ int or_head_stats(int64_t R, int64_t d, int64_t V, int dtype,
                   const void* h, const float* h_scale,
                   const void* w, const float* w_scale, double inv_temp,
                   const int64_t* rows, int64_t n_rows,
-                  int32_t* argmax, double* conf, double* entropy, double* gap2) {
+                  int32_t* argmax, double* conf, double* entropy, double* gap2,
+                  const uint8_t* h_bscale, const uint8_t* w_bscale) {
     if (R < 0 || d <= 0 || V <= 0 || n_rows < 0) return -1;
-    if (dtype == OR_E4M3 && (!h_scale || !w_scale)) return -1;
+    if ((dtype == OR_E4M3 || dtype == OR_NVFP4) && (!h_scale || !w_scale)) return -1;
+    if (dtype == OR_NVFP4 && (d % 16 != 0 || !h_bscale || !w_bscale)) return -1;
+    const int scaled = dtype == OR_E4M3 || dtype == OR_NVFP4;
     const int64_t RB = 256;                     /* rows per block: bounds the logit buffer */
     double* L = (double*)malloc(sizeof(double) * (size_t)(RB * V));
     double* hd = (double*)malloc(sizeof(double) * (size_t)(RB * d));
@@ -177,16 +267,18 @@ int or_head_stats(int64_t R, int64_t d, int64_t V, int dtype,
         int64_t nb = n_rows - b0 < RB ? n_rows - b0 : RB;
         for (int64_t i = 0; i < nb; i++) {
             int64_t r = rows ? rows[b0 + i] : b0 + i;
-            for (int64_t k = 0; k < d; k++) hd[i * d + k] = operand(dtype, h, r * d + k);
-            hs[i] = (dtype == OR_E4M3) ? (double)h_scale[r] : 1.0;
+            for (int64_t k = 0; k < d; k++)
+                hd[i * d + k] = operand(dtype, h, r * d + k) * block_scale(dtype, h_bscale, r, d, k);
+            hs[i] = scaled ? (double)h_scale[r] : 1.0;
         }
         #pragma omp parallel
         {
             double* wd = (double*)malloc(sizeof(double) * (size_t)d);
             #pragma omp for schedule(static)
             for (int64_t n = 0; n < V; n++) {
-                for (int64_t k = 0; k < d; k++) wd[k] = operand(dtype, w, n * d + k);
-                double ws = (dtype == OR_E4M3) ? (double)w_scale[n] : 1.0;
+                for (int64_t k = 0; k < d; k++)
+                    wd[k] = operand(dtype, w, n * d + k) * block_scale(dtype, w_bscale, n, d, k);
+                double ws = scaled ? (double)w_scale[n] : 1.0;
                 for (int64_t i = 0; i < nb; i++) {
                     double acc = 0.0;
                     const double* hr = hd + i * d;
@@ -371,4 +463,11 @@ void or_e4m3_round_many(const float* x, int64_t n, uint8_t* out) {
 
 void or_e4m3_value_many(const uint8_t* q, int64_t n, double* out) {
     for (int64_t i = 0; i < n; i++) out[i] = or_e4m3_value(q[i]);
+}
+
+void or_e2m1_round_many(const float* x, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; i++) out[i] = or_e2m1_round_satfinite(x[i]);
+}
+void or_e2m1_value_many(const uint8_t* q, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; i++) out[i] = or_e2m1_value(q[i]);
 }

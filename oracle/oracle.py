@@ -23,9 +23,9 @@ from pathlib import Path
 
 import numpy as np
 
-OR_F32, OR_BF16, OR_E4M3 = 0, 1, 2
-_DT = {"f32": OR_F32, "bf16": OR_BF16, "e4m3": OR_E4M3, OR_F32: OR_F32, OR_BF16: OR_BF16,
-       OR_E4M3: OR_E4M3}
+OR_F32, OR_BF16, OR_E4M3, OR_NVFP4 = 0, 1, 2, 3
+_DT = {"f32": OR_F32, "bf16": OR_BF16, "e4m3": OR_E4M3, "nvfp4": OR_NVFP4, OR_F32: OR_F32,
+       OR_BF16: OR_BF16, OR_E4M3: OR_E4M3, OR_NVFP4: OR_NVFP4}
 
 INIT_PASS = 0xFFFFFFFF          # hash pass index of the initial random canvas
 REASON_ENTROPY, REASON_STABLE, REASON_CAP = 1, 2, 4
@@ -53,7 +53,7 @@ def _L():
         lib = C.CDLL(str(build()))
         i64, u64, u32, vp, dbl = C.c_int64, C.c_uint64, C.c_uint32, C.c_void_p, C.c_double
         lib.or_head_stats.argtypes = [i64, i64, i64, C.c_int, vp, vp, vp, vp, dbl, vp, i64,
-                                      vp, vp, vp, vp]
+                                      vp, vp, vp, vp, vp, vp]
         lib.or_head_stats.restype = C.c_int
         lib.or_select.argtypes = [i64, i64, i64, vp, vp, vp, i64, u64, u32, C.c_int, i64, u64,
                                   vp, vp, vp, vp]
@@ -70,6 +70,9 @@ def _L():
         lib.or_e4m3_round_many.argtypes = [vp, i64, vp]
         lib.or_e4m3_value_many.argtypes = [vp, i64, vp]
         lib.or_quant_rows_e4m3.argtypes = [vp, i64, i64, vp, vp]
+        lib.or_quant_rows_nvfp4.argtypes = [vp, i64, i64, vp, vp, vp]
+        lib.or_e2m1_round_many.argtypes = [vp, i64, vp]
+        lib.or_e2m1_value_many.argtypes = [vp, i64, vp]
         lib.or_synth_denoise.argtypes = [i64, i64, i64, i64, C.c_int, vp, vp, vp, vp, u32, i64,
                                          dbl, dbl, vp]
         lib.or_synth_denoise.restype = C.c_int
@@ -87,7 +90,13 @@ def _c(a, dt):
 
 
 def _operand(dtype: int, a):
-    return _c(a, {OR_F32: np.float32, OR_BF16: np.uint16, OR_E4M3: np.uint8}[dtype])
+    return _c(a, {OR_F32: np.float32, OR_BF16: np.uint16, OR_E4M3: np.uint8,
+                  OR_NVFP4: np.uint8}[dtype])
+
+
+def _elems(dtype: int, a) -> int:
+    """Number of operand elements in a stored array (NVFP4 packs two per byte)."""
+    return a.size * 2 if dtype == OR_NVFP4 else a.size
 
 
 def num_threads() -> int:
@@ -147,16 +156,47 @@ def quant_rows_e4m3(h_bf16, rows: int, d: int):
     return q, sc
 
 
+def e2m1_round(x) -> np.ndarray:
+    """FP4 E2M1 codes (4-bit, one per byte) of float32 values, nearest-even, saturating."""
+    x = _c(x, np.float32)
+    out = np.empty(x.size, np.uint8)
+    _L().or_e2m1_round_many(_p(x), x.size, _p(out))
+    return out
+
+
+def e2m1_value(q) -> np.ndarray:
+    q = _c(q, np.uint8)
+    out = np.empty(q.size, np.float64)
+    _L().or_e2m1_value_many(_p(q), q.size, _p(out))
+    return out
+
+
+def quant_rows_nvfp4(h_bf16, rows: int, d: int):
+    """NVFP4 quantisation of bf16 rows -> (packed E2M1 codes [rows*d/2], E4M3 block scales
+    [rows*d/16], fp32 row scales [rows])."""
+    h = _c(h_bf16, np.uint16)
+    assert h.size == rows * d and d % 16 == 0
+    q = np.empty(rows * d // 2, np.uint8)
+    bs = np.empty(rows * d // 16, np.uint8)
+    sc = np.empty(rows, np.float32)
+    _L().or_quant_rows_nvfp4(_p(h), rows, d, _p(q), _p(bs), _p(sc))
+    return q, bs, sc
+
+
 # ---------------------------------------------------------------------------------------------
 # one pass
 # ---------------------------------------------------------------------------------------------
 def head_stats(R: int, d: int, V: int, dtype, h, w, h_scale=None, w_scale=None,
-               rows=None, inv_temp: float = 1.0) -> dict:
-    """argmax, conf = max p, entropy H (nats) and the top-2 logit gap for rows of h."""
+               rows=None, inv_temp: float = 1.0, h_bscale=None, w_bscale=None) -> dict:
+    """argmax, conf = max p, entropy H (nats) and the top-2 logit gap for rows of h.
+    NVFP4 operands: packed E2M1 codes, per-row fp32 scales and per-16 E4M3 block scales
+    [rows][d/16] (h_bscale, w_bscale)."""
     dt = _DT[dtype]
     h = _operand(dt, h)
     w = _operand(dt, w)
-    assert h.size == R * d and w.size == V * d
+    assert _elems(dt, h) == R * d and _elems(dt, w) == V * d
+    hb = None if h_bscale is None else _c(h_bscale, np.uint8)
+    wb = None if w_bscale is None else _c(w_bscale, np.uint8)
     hs = None if h_scale is None else _c(h_scale, np.float32)
     ws = None if w_scale is None else _c(w_scale, np.float32)
     rr = None if rows is None else _c(rows, np.int64)
@@ -165,7 +205,7 @@ def head_stats(R: int, d: int, V: int, dtype, h, w, h_scale=None, w_scale=None,
            "entropy": np.empty(n, np.float64), "gap2": np.empty(n, np.float64)}
     rc = _L().or_head_stats(R, d, V, dt, _p(h), _p(hs), _p(w), _p(ws), float(inv_temp), _p(rr),
                             n, _p(out["argmax"]), _p(out["conf"]), _p(out["entropy"]),
-                            _p(out["gap2"]))
+                            _p(out["gap2"]), _p(hb), _p(wb))
     if rc != 0:
         raise RuntimeError(f"or_head_stats failed: {rc}")
     return out
@@ -194,15 +234,21 @@ def select(B: int, S: int, V: int, argmax, conf, entropy, keep_k: int, seed: int
 
 def step(B: int, S: int, V: int, d: int, dtype, h, w, keep_k: int, seed: int, pass_: int,
          h_scale=None, w_scale=None, inv_temp: float = 1.0, keep_rule: int = 0,
-         mask_id: int = -1, row_offset: int = 0) -> dict:
-    """One canvas pass. For an E4M3 head given bf16 h, h is first quantised per row."""
+         mask_id: int = -1, row_offset: int = 0, h_bscale=None, w_bscale=None) -> dict:
+    """One canvas pass. For an E4M3 or NVFP4 head given bf16 h, h is first quantised per row
+    with the head's rule."""
     dt = _DT[dtype]
     out = {}
     if dt == OR_E4M3 and h_scale is None:
         q, sc = quant_rows_e4m3(h, B * S, d)
         h, h_scale = q, sc
         out["q_h"], out["sc_h"] = q, sc
-    st = head_stats(B * S, d, V, dt, h, w, h_scale, w_scale, inv_temp=inv_temp)
+    if dt == OR_NVFP4 and h_scale is None:
+        q, bsc, sc = quant_rows_nvfp4(h, B * S, d)
+        h, h_bscale, h_scale = q, bsc, sc
+        out["q_h"], out["bsc_h"], out["sc_h"] = q, bsc, sc
+    st = head_stats(B * S, d, V, dt, h, w, h_scale, w_scale, inv_temp=inv_temp,
+                    h_bscale=h_bscale, w_bscale=w_bscale)
     sel = select(B, S, V, st["argmax"], st["conf"], st["entropy"], keep_k, seed, pass_,
                  keep_rule=keep_rule, mask_id=mask_id, row_offset=row_offset)
     out.update(st)

@@ -110,3 +110,82 @@ def test_quant_rows_error_bound_and_amax(orc):
     err = np.abs(deq - hv)
     bound = np.maximum(np.abs(hv) * 2.0**-4, 2.0**-10 * sc.astype(np.float64)[:, None]) * 1.0001
     assert (err <= bound + 1e-12 * amax[:, None]).all()
+
+
+def test_e2m1_published_encodings(orc):
+    rows = []
+    with open(os.path.join(GOLDEN, "e2m1_kat.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                code, val = line.split()
+                rows.append((int(code, 16), float(val)))
+    assert len(rows) == 16
+    got = orc.e2m1_value(np.array([c for c, _ in rows], np.uint8))
+    for (code, val), g in zip(rows, got):
+        assert g == val and np.signbit(g) == np.signbit(val), hex(code)
+
+
+def _e2m1_nearest_even(x):
+    """Brute force: the E2M1 code whose value is nearest to x, ties to the even code (mantissa
+    bit 0), magnitudes beyond 6 saturated to 6."""
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    s = 0x8 if np.signbit(x) else 0
+    a = min(abs(float(x)), 6.0)
+    best = min(range(8), key=lambda c: (abs(mags[c] - a), c & 1))
+    return s | best
+
+
+def test_e2m1_rounding_brute_force(orc):
+    # a dense grid covering every interval, every midpoint exactly, values past saturation, and
+    # random fp32 values of both signs
+    grid = np.arange(-8.0, 8.0, 0.0625, dtype=np.float32)
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    rng = np.random.default_rng(3)
+    x = np.concatenate([grid, mids, -mids, np.nextafter(mids, 0), np.nextafter(mids, 10),
+                        (rng.standard_normal(20000) * 3).astype(np.float32),
+                        np.array([1e-30, -1e-30, 100.0, -1e6], np.float32)])
+    got = orc.e2m1_round(x)
+    want = np.array([_e2m1_nearest_even(v) for v in x], np.uint8)
+    assert np.array_equal(got, want)
+
+
+def _bf16(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_nvfp4_quantiser_hand_row_and_roundtrip(orc):
+    # one row of 32 elements = two blocks. Block 0 holds exact grid values times 0.25 with amax 6
+    # times 0.25 = 1.5 (the row max): g = 1.5 / 2688, block scale = 1.5 / (6 g) = 448 exactly
+    # (E4M3 0x7E), codes equal the grid codes. Block 1 is all zero: scale 0, codes 0.
+    vals = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6, -0.5, -1, -1.5, -2, -3, -4, -6, 6], np.float32) * 0.25
+    row = np.concatenate([vals, np.zeros(16, np.float32)])
+    q, bs, sc = orc.quant_rows_nvfp4(_bf16(row), 1, 32)
+    assert sc[0] == np.float32(1.5) / np.float32(2688)
+    assert bs[0] == 0x7E and bs[1] == 0
+    codes = np.stack([q & 0xF, q >> 4], axis=1).reshape(-1)
+    assert list(codes[:16]) == [0, 1, 2, 3, 4, 5, 6, 7, 9, 10, 11, 12, 13, 14, 15, 7]
+    assert not codes[16:].any()
+    # decoded values e2m1 * value(block scale) * g reproduce the row within fp32 rounding
+    dec = orc.e2m1_value(codes[:16]) * orc.e4m3_value(bs[:1])[0] * float(sc[0])
+    assert np.allclose(dec, vals.astype(np.float64), rtol=1e-6, atol=0)
+    # an all-zero row: scale 1, every block scale and code 0
+    q, bs, sc = orc.quant_rows_nvfp4(np.zeros(32, np.uint16), 1, 32)
+    assert sc[0] == 1.0 and not bs.any() and not q.any()
+
+
+def test_nvfp4_quantiser_error_bound(orc):
+    # every element lies within half a step of the E2M1 grid scaled by its block: the error is at
+    # most 0.25 * value(block scale) * g below magnitude 2 (step 0.5), 0.5 up to 4, 1 up to 6
+    rng = np.random.default_rng(11)
+    R, d = 8, 64
+    h = (rng.standard_normal(R * d) * np.exp(rng.standard_normal(R * d))).astype(np.float32)
+    hb = _bf16(h)
+    x = ((hb.astype(np.uint32) << 16).view(np.float32)).astype(np.float64).reshape(R, d)
+    q, bs, sc = orc.quant_rows_nvfp4(hb, R, d)
+    codes = np.stack([q & 0xF, q >> 4], axis=1).reshape(R, d)
+    unit = orc.e4m3_value(bs).reshape(R, d // 16).repeat(16, axis=1) * sc[:, None].astype(np.float64)
+    dec = orc.e2m1_value(codes.reshape(-1)).reshape(R, d) * unit
+    mag = np.abs(x) / np.where(unit > 0, unit, 1)
+    step = np.where(mag < 2, 0.5, np.where(mag < 4, 1.0, 2.0))
+    assert (np.abs(dec - x) <= step / 2 * unit * (1 + 1e-6) + 1e-300).all()

@@ -177,3 +177,27 @@ def test_scales_multiply_logits(orc):
     for r in range(R):
         assert got["argmax"][r] == ref[r][0]
         assert abs(got["entropy"][r] - ref[r][2]) < 1e-12
+
+
+@pytest.mark.parametrize("V,d,R", [(1, 16, 2), (5, 16, 3), (17, 32, 4)])
+def test_brute_force_small_nvfp4(orc, V, d, R):
+    """NVFP4 operands: each element is e2m1(code) * value(block scale) * row scale; the oracle's
+    statistics against the exact rational contraction of those values."""
+    rng = np.random.default_rng(V * 7 + d + R)
+    h = (rng.standard_normal(R * d) * 1.5).astype(np.float32)
+    w = rng.standard_normal(V * d).astype(np.float32)
+    hq, hb, hs = orc.quant_rows_nvfp4(_bf16_bits(h), R, d)
+    wq, wb, ws = orc.quant_rows_nvfp4(_bf16_bits(w), V, d)
+
+    def values(q, b, rows):
+        codes = np.stack([q & 0xF, q >> 4], axis=1).reshape(-1)
+        return orc.e2m1_value(codes) * orc.e4m3_value(b).repeat(16)
+
+    got = orc.head_stats(R, d, V, "nvfp4", hq, wq, h_scale=hs, w_scale=ws, h_bscale=hb, w_bscale=wb)
+    ref = _brute([float(x) for x in values(hq, hb, R)], [float(x) for x in values(wq, wb, V)],
+                 R, d, V, hs, ws)
+    for r in range(R):
+        a, conf, H, gap = ref[r]
+        assert got["argmax"][r] == a
+        assert abs(got["conf"][r] - conf) < 1e-12
+        assert abs(got["entropy"][r] - H) < 1e-12
