@@ -129,9 +129,13 @@ def to_dev_bf16(bits, shape):
 
 def algorithmic(cfg):
     """FLOPs and algorithmic bytes of one pass (operands read once, O(R) outputs)."""
-    eb = {"f32": 4, "bf16": 2, "e4m3": 1}[cfg.precision]
     flops = 2.0 * cfg.R * cfg.V * cfg.d
-    byts = cfg.V * cfg.d * eb + cfg.R * cfg.d * eb + cfg.R * (4 + 4 + 4 + 1 + 4)
+    out_bytes = cfg.R * (4 + 4 + 4 + 1 + 4)
+    if cfg.precision == "nvfp4":
+        # W codes (4 bits) + E4M3 block scales (1 per 16) + fp32 row scales; bf16 h in
+        return flops, cfg.V * cfg.d / 2 + cfg.V * cfg.d / 16 + cfg.V * 4 + cfg.R * cfg.d * 2 + out_bytes
+    eb = {"f32": 4, "bf16": 2, "e4m3": 1}[cfg.precision]
+    byts = cfg.V * cfg.d * eb + cfg.R * cfg.d * eb + out_bytes
     if cfg.precision == "e4m3":
         byts += cfg.V * 4 + cfg.R * 4
     return flops, byts
@@ -173,7 +177,8 @@ def roofline(cfg, r, peaks, peak_kind, step_s):
     fp8/bf16 ratio); the HBM peak is the measured copy bandwidth."""
     head_s = statistics.mean(r["head_ms"]) / 1e3
     fp8 = cfg.precision == "e4m3"
-    ratio = 2.0 if fp8 else 1.0
+    # nominal dense tensor rates relative to bf16: E4M3 2x, NVFP4 6x (13.5 vs 2.25 PFLOP/s)
+    ratio = {"e4m3": 2.0, "nvfp4": 6.0}.get(cfg.precision, 1.0)
     tens = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * ratio
     t_mem = r["bytes"] / (peaks["hbm_gbs"] * 1e9)
     t_flop = r["flops"] / (tens * 1e12)
@@ -186,12 +191,14 @@ def roofline(cfg, r, peaks, peak_kind, step_s):
     else:
         achieved = r["flops"] / head_s / 1e12
         out.update(bound="tensor", achieved=achieved, peak=tens, unit="TFLOP/s", frac=achieved / tens,
-                   peak_source=f"{peak_kind} sustained bf16 cuBLAS" + (" x2 nominal fp8/bf16" if fp8 else ""))
+                   peak_source=f"{peak_kind} sustained bf16 cuBLAS" +
+                   (f" x{ratio:g} nominal {cfg.precision}/bf16" if ratio != 1.0 else ""))
     rec = TRAFFIC.get(cfg.name)
     out["traffic"] = rec["bytes"] if rec and rec["src"] == head_source_hash() else None
-    out["kernel"] = {"f32": "head_simt_kernel", "bf16": "head_tc2_kernel<0>",
-                     "e4m3": "head_tc2_kernel<1>"}[cfg.precision] if cfg.R > 128 or cfg.precision == "f32" \
-        else {"bf16": "head_tc_kernel<0>", "e4m3": "head_tc_kernel<1>"}[cfg.precision]
+    out["kernel"] = ("head_fp4_kernel" if cfg.precision == "nvfp4" else
+                     {"f32": "head_simt_kernel", "bf16": "head_tc2_kernel<0>",
+                      "e4m3": "head_tc2_kernel<1>"}[cfg.precision] if cfg.R > 128 or cfg.precision == "f32"
+                     else {"bf16": "head_tc_kernel<0>", "e4m3": "head_tc_kernel<1>"}[cfg.precision])
     out["kernel_us"] = head_s * 1e6
     out["t_roof_us"] = max(t_mem, t_flop) * 1e6
     out["roof_frac"] = max(t_mem, t_flop) / head_s
@@ -199,7 +206,7 @@ def roofline(cfg, r, peaks, peak_kind, step_s):
     out["tensor_frac_sustained"] = r["flops"] / head_s / 1e12 / tens
     out["tensor_frac_burst"] = r["flops"] / head_s / 1e12 / (peaks["bf16_tflops"] * ratio)
     ds_t = max(r["bytes"] / (DATASHEET["hbm_gbs"] * 1e9),
-               r["flops"] / ((DATASHEET["e4m3_tflops"] if fp8 else DATASHEET["bf16_tflops"]) * 1e12))
+               r["flops"] / (DATASHEET["bf16_tflops"] * ratio * 1e12))
     out["datasheet_roof_frac"] = ds_t / head_s
     out["step_roof_frac"] = max(t_mem, t_flop) / step_s
     return out
@@ -236,14 +243,21 @@ def run_ours(args, cfg, ws_, rank):
     stream = torch.cuda.current_stream()
     flops, byts = algorithmic(cfg)
     R, d, V = cfg.R, cfg.d, cfg.V
-    launches_per_step = 2 + (1 if cfg.precision == "e4m3" else 0)
+    launches_per_step = 2 + (1 if cfg.precision in ("e4m3", "nvfp4") else 0)
 
     if cfg.mode == "pass":
         x = make_pass_inputs(cfg)
+        dkw = {}
         if cfg.precision == "f32":
             h = torch.from_numpy(x["h"]).view(R, d).cuda()
             w = torch.from_numpy(x["w"]).view(V, d).cuda()
             wsc = None
+        elif cfg.precision == "nvfp4":
+            h = to_dev_bf16(x["h"], (R, d))
+            w = torch.from_numpy(x["w"]).view(V, d // 2).cuda()
+            wsc = torch.from_numpy(x["w_scale"]).cuda()
+            wbs = dg.dg_nvfp4_pack_scales(torch.from_numpy(x["w_bscale"]).view(V, d // 16).cuda(), V, d)
+            dkw = dict(w_dtype=dg.DG_NVFP4, w_block_scale=wbs)
         elif cfg.precision == "bf16":
             h, w, wsc = to_dev_bf16(x["h"], (R, d)), to_dev_bf16(x["w"], (V, d)), None
         else:
@@ -256,7 +270,7 @@ def run_ours(args, cfg, ws_, rank):
         state = dg.new_state(cfg.B, dev)
         rule = dg.StopRule(max_passes=1 << 30, entropy_threshold=0.0, stable_passes=1 << 30,
                            stop_mode=dg.STOP_OR)
-        desc = dg.make_desc(h, w, B=cfg.B, S=cfg.S, w_scale=wsc)
+        desc = dg.make_desc(h, w, B=cfg.B, S=cfg.S, w_scale=wsc, **dkw)
         wsb = torch.empty(dg.dg_workspace_bytes(desc) + 256, dtype=torch.uint8, device=dev)
         status = torch.zeros(1, dtype=torch.int32, device=dev)
         outs = {"argmax": torch.empty(R, dtype=torch.int32, device=dev),
@@ -432,17 +446,21 @@ def oracle_sample(cfg, target_s: float = 15.0):
     h = normal_f32(R * d, cfg.seed, TAG_H)
     if cfg.precision != "f32":
         h = f32_to_bf16_bits(h)
-    hs = None
+    hs = hb = None
     if cfg.precision == "e4m3":
         h, hs = oracle.quant_rows_e4m3(h, R, d)
+    if cfg.precision == "nvfp4":
+        h, hb, hs = oracle.quant_rows_nvfp4(h, R, d)
+    bkw = {} if cfg.precision != "nvfp4" else dict(h_bscale=hb, w_bscale=head["w_bscale"])
     # calibrate with one row, then size the sample to roughly target_s seconds
     t0 = time.perf_counter()
-    oracle.head_stats(R, d, V, cfg.precision, h, w, h_scale=hs, w_scale=wsc, rows=np.arange(rows))
+    oracle.head_stats(R, d, V, cfg.precision, h, w, h_scale=hs, w_scale=wsc, rows=np.arange(rows),
+                      **bkw)
     t1 = time.perf_counter() - t0
     rows = int(max(1, min(R, target_s / max(t1, 1e-6))))
     t0 = time.perf_counter()
     st = oracle.head_stats(R, d, V, cfg.precision, h, w, h_scale=hs, w_scale=wsc,
-                           rows=np.arange(rows))
+                           rows=np.arange(rows), **bkw)
     t_stats = time.perf_counter() - t0
     # the per-canvas step on the full canvas (cheap): reuse the sampled rows' stats cyclically
     idx = np.arange(R) % rows
@@ -472,7 +490,7 @@ def main():
     workload = {"workload": cfg.name, "canvases": cfg.B, "slots": cfg.S, "vocab": cfg.V,
                 "hidden": cfg.d, "precision": cfg.precision, "mode": cfg.mode,
                 "keep_k": cfg.keep_k, "seed": cfg.seed,
-                "l2": "inputs larger than L2 (head %.2f GB)" % (cfg.V * cfg.d * {"f32": 4, "bf16": 2, "e4m3": 1}[cfg.precision] / 1e9)
+                "l2": "inputs larger than L2 (head %.2f GB)" % (cfg.V * cfg.d * {"f32": 4, "bf16": 2, "e4m3": 1, "nvfp4": 0.5625}[cfg.precision] / 1e9)
                 if cfg.V * cfg.d > L2_BYTES else "L2-resident head, latency-bound"}
 
     if args.impl == "reference":
@@ -516,7 +534,7 @@ def main():
     line = {"metric": metric, "value": value, "unit": "canvas passes/s", "n_gpus": ws_,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": {"f32": "f32", "bf16": "bf16", "e4m3": "e4m3"}[cfg.precision],
+            "dtype": {"f32": "f32", "bf16": "bf16", "e4m3": "e4m3", "nvfp4": "nvfp4"}[cfg.precision],
             "data": "synthetic (seeded N(0,1) hidden states, N(0,1/d) head)",
             "config": workload, "slots_per_s": value * cfg.S,
             "e2e": {"value": e2e, "unit": "canvas passes/s", "h2d_bytes_per_step": r["h2d"],

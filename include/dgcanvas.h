@@ -56,7 +56,7 @@ extern "C" {
 
 typedef struct CUstream_st* dg_stream_t; /* identical to cudaStream_t */
 
-typedef enum { DG_F32 = 0, DG_BF16 = 1, DG_E4M3 = 2 } dg_dtype;
+typedef enum { DG_F32 = 0, DG_BF16 = 1, DG_E4M3 = 2, DG_NVFP4 = 3 } dg_dtype;
 
 enum {
     DG_OK = 0,
@@ -97,7 +97,14 @@ enum { DG_REDRAW_UNIFORM = 0, DG_REDRAW_MASK = 1 };
  * Supported (h_dtype, w_dtype): (F32, F32) on CUDA cores; (BF16, BF16) and (E4M3, E4M3) on the
  * tensor cores; (BF16, E4M3) quantises h per row to E4M3 first (absmax scaling:
  * scale = amax/448, q = e4m3_rn_satfinite(h * (448/amax)), all in fp32; amax = 0 gives scale 1).
- * Limits: 1 <= S <= 1024, B >= 1, 1 <= V < 2^31, d >= 1 with d*elem_size(dtype) % 16 == 0.
+ * NVFP4 (4-bit; the NVFP4-quantised variant of the laura-martel.com page, introduction):
+ * (NVFP4, NVFP4) and (BF16, NVFP4), the latter quantising h on the device with dg_quantize_nvfp4's
+ * rule. An NVFP4 operand is three arrays: E2M1 codes [rows, d/2] bytes (element 2j in the low
+ * nibble of byte j), the fp32 row scale (h_scale / w_scale) and E4M3 block scales, one per 16
+ * elements along d, in the packed layout of dg_nvfp4_pack_scales (h_block_scale /
+ * w_block_scale); element value = e2m1(code) * e4m3(block scale) * row scale.
+ * Limits: 1 <= S <= 1024, B >= 1, 1 <= V < 2^31, d >= 1 with d*elem_size(dtype) % 16 == 0
+ * (elem_size 4 / 2 / 1 / 0.5); NVFP4 also needs d % 256 == 0.
  */
 typedef struct {
     int32_t B, S, d, V;
@@ -107,6 +114,8 @@ typedef struct {
     const void* w;
     const float* w_scale;
     float inv_temp;           /* 1.0f = untempered statistics */
+    const uint8_t* h_block_scale;  /* NVFP4 h: packed E4M3 block scales, else NULL */
+    const uint8_t* w_block_scale;  /* NVFP4 w: packed E4M3 block scales, else NULL */
 } dg_head_desc;
 
 /* Per-canvas loop state in device memory (32 bytes per canvas). */
@@ -262,6 +271,28 @@ DG_API int dg_block_generate(const dg_head_desc* desc, int32_t n_blocks, const i
                              float s_content, float s_pad, int32_t* tokens_out,
                              dg_canvas_state* states_out, void* workspace, size_t workspace_bytes,
                              uint32_t* status, dg_stream_t stream);
+
+/*
+ * NVFP4 operand preparation (4-bit heads).
+ *   dg_nvfp4_scale_bytes: size of the packed block-scale array of `rows` rows of width d:
+ *     ceil(rows / 256) * 256 * d / 16 bytes.
+ *   dg_nvfp4_pack_scales: block scales [rows, d/16] (row-major, E4M3) -> the packed layout the
+ *     block-scaled MMA consumes: one 512-byte atom per (128-row group g, 64-element step j) at
+ *     offset (g * d/64 + j) * 512, byte (m % 32) * 16 + (m / 32) * 4 + kb holding row 128 g + m,
+ *     block 4 j + kb; rows past `rows` are zero. Device pointers, d % 64 == 0.
+ *   dg_quantize_nvfp4: two-level NVFP4 quantisation of bf16 rows [rows, d] on the device, in
+ *     IEEE binary32: amax = max |h|; amax == 0 gives row scale 1 and zero codes / block scales;
+ *     else g = amax / 2688, per block of 16: sb = e4m3_rn_satfinite(bmax / (6 g)), codes
+ *     q = e2m1_rn_satfinite(h / (value(sb) g)) (0 where sb = 0). Writes codes [rows, d/2], packed
+ *     block scales (dg_nvfp4_scale_bytes) and row scales [rows]. Sets DG_ST_NONFINITE on
+ *     non-finite input. d % 64 == 0.
+ */
+DG_API int dg_nvfp4_scale_bytes(int32_t rows, int32_t d, size_t* bytes);
+DG_API int dg_nvfp4_pack_scales(const uint8_t* block_scales, int32_t rows, int32_t d,
+                                uint8_t* packed, dg_stream_t stream);
+DG_API int dg_quantize_nvfp4(const void* h_bf16, int32_t rows, int32_t d, uint8_t* codes,
+                             uint8_t* block_scale_packed, float* row_scale, uint32_t* status,
+                             dg_stream_t stream);
 
 /*
  * dg_canvas_step without a caller-supplied workspace, for callers that cannot allocate device

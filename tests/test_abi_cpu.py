@@ -47,7 +47,7 @@ def test_struct_layouts_match_header(dg):
 int main(void) {
   printf("dg_head_desc %zu\n", sizeof(dg_head_desc));
   P(dg_head_desc, h) P(dg_head_desc, h_scale) P(dg_head_desc, w) P(dg_head_desc, w_scale)
-  P(dg_head_desc, inv_temp)
+  P(dg_head_desc, inv_temp) P(dg_head_desc, h_block_scale) P(dg_head_desc, w_block_scale)
   printf("dg_canvas_state %zu\n", sizeof(dg_canvas_state));
   printf("dg_stop_rule %zu\n", sizeof(dg_stop_rule));
   printf("dg_loop_params %zu\n", sizeof(dg_loop_params));

@@ -21,9 +21,10 @@ __all__ = ["DG_F32", "DG_BF16", "DG_E4M3", "HeadDesc", "CanvasState", "StopRule"
            "dg_canvas_step", "dg_canvas_loop", "dg_status_string", "dtype_code", "new_state",
            "REASON_ENTROPY", "REASON_STABLE", "REASON_CAP", "ST_BAD_TOKEN", "ST_NONFINITE",
            "ST_TIMEOUT", "STOP_OR", "STOP_AND", "KEEP_CONFIDENCE", "KEEP_ENTROPY",
-           "REDRAW_UNIFORM", "REDRAW_MASK", "pass_rule", "dg_block_generate", "timeline_us"]
+           "REDRAW_UNIFORM", "REDRAW_MASK", "pass_rule", "dg_block_generate", "timeline_us",
+           "DG_NVFP4", "nvfp4_scale_bytes", "dg_nvfp4_pack_scales", "dg_quantize_nvfp4"]
 
-DG_F32, DG_BF16, DG_E4M3 = 0, 1, 2
+DG_F32, DG_BF16, DG_E4M3, DG_NVFP4 = 0, 1, 2, 3
 DG_TL_DENOISE, DG_TL_HEAD, DG_TL_MERGE, DG_TL_KERNELS = 0, 1, 2, 3
 REASON_ENTROPY, REASON_STABLE, REASON_CAP = 1, 2, 4
 ST_BAD_TOKEN, ST_NONFINITE, ST_TIMEOUT = 1, 2, 4
@@ -45,7 +46,8 @@ class HeadDesc(C.Structure):
     _fields_ = [("B", C.c_int32), ("S", C.c_int32), ("d", C.c_int32), ("V", C.c_int32),
                 ("h_dtype", C.c_int32), ("w_dtype", C.c_int32), ("h", C.c_void_p),
                 ("h_scale", C.c_void_p), ("w", C.c_void_p), ("w_scale", C.c_void_p),
-                ("inv_temp", C.c_float)]
+                ("inv_temp", C.c_float), ("h_block_scale", C.c_void_p),
+                ("w_block_scale", C.c_void_p)]
 
 
 class CanvasState(C.Structure):
@@ -96,6 +98,11 @@ def lib():
         L.dg_status_string.argtypes = [C.c_int]
         L.dg_status_string.restype = C.c_char_p
         L.dg_version.restype = C.c_int
+        L.dg_nvfp4_scale_bytes.argtypes = [C.c_int32, C.c_int32, C.POINTER(sz)]
+        L.dg_nvfp4_pack_scales.argtypes = [vp, C.c_int32, C.c_int32, vp, vp]
+        L.dg_quantize_nvfp4.argtypes = [vp, C.c_int32, C.c_int32, vp, vp, vp, vp, vp]
+        for f in ("dg_nvfp4_scale_bytes", "dg_nvfp4_pack_scales", "dg_quantize_nvfp4"):
+            getattr(L, f).restype = C.c_int
         L.dg_block_generate.argtypes = [C.POINTER(HeadDesc), C.c_int32, vp, vp, vp, vp, vp,
                                         C.POINTER(LoopParams), C.c_int32, C.c_float, C.c_float,
                                         vp, vp, vp, sz, vp, vp]
@@ -152,16 +159,26 @@ def _stream(stream):
 
 
 def make_desc(h, w, *, B: int, S: int, h_scale=None, w_scale=None, inv_temp: float = 1.0,
-              h_dtype: int | None = None, d: int | None = None) -> HeadDesc:
+              h_dtype: int | None = None, d: int | None = None, w_dtype: int | None = None,
+              h_block_scale=None, w_block_scale=None) -> HeadDesc:
     """Head descriptor over torch tensors: h [B*S, d] (or None for a loop's buffer later),
-    w [V, d], optional fp32 scales for E4M3 operands."""
+    w [V, d], optional fp32 scales for E4M3 / NVFP4 operands. NVFP4 operands are uint8 code
+    tensors [rows, d/2] with w_dtype / h_dtype = DG_NVFP4 and packed block scales."""
     V, dd = int(w.shape[0]), int(w.shape[1])
-    hd = dtype_code(h) if h is not None else (DG_BF16 if h_dtype is None else h_dtype)
-    return HeadDesc(B=B, S=S, d=dd if d is None else d, V=V, h_dtype=hd, w_dtype=dtype_code(w),
+    wd = dtype_code(w) if w_dtype is None else w_dtype
+    if wd == DG_NVFP4:
+        dd *= 2
+    hd = (h_dtype if h_dtype is not None else dtype_code(h)) if h is not None else \
+        (DG_BF16 if h_dtype is None else h_dtype)
+    d_ = dd if d is None else d
+    desc = HeadDesc(B=B, S=S, d=d_, V=V, h_dtype=hd, w_dtype=wd,
                     h=None if h is None else _ptr(h).value, h_scale=None if h_scale is None else
                     _ptr(h_scale).value, w=_ptr(w).value,
                     w_scale=None if w_scale is None else _ptr(w_scale).value,
                     inv_temp=float(inv_temp))
+    desc.h_block_scale = None if h_block_scale is None else _ptr(h_block_scale).value
+    desc.w_block_scale = None if w_block_scale is None else _ptr(w_block_scale).value
+    return desc
 
 
 def dg_workspace_bytes(desc: HeadDesc) -> int:
@@ -184,12 +201,41 @@ def new_state(B: int, device) -> torch.Tensor:
     return torch.zeros(B, 8, dtype=torch.int32, device=device)
 
 
+def nvfp4_scale_bytes(rows: int, d: int) -> int:
+    n = C.c_size_t(0)
+    _check(lib().dg_nvfp4_scale_bytes(int(rows), int(d), C.byref(n)), "dg_nvfp4_scale_bytes")
+    return int(n.value)
+
+
+def dg_nvfp4_pack_scales(block_scales, rows: int, d: int, stream=None) -> torch.Tensor:
+    """Plain E4M3 block scales [rows, d/16] (uint8, device) -> the packed layout NVFP4 heads read."""
+    out = torch.empty(nvfp4_scale_bytes(rows, d), dtype=torch.uint8, device=block_scales.device)
+    _check(lib().dg_nvfp4_pack_scales(_ptr(block_scales), int(rows), int(d), _ptr(out),
+                                      _stream(stream)), "dg_nvfp4_pack_scales")
+    return out
+
+
+def dg_quantize_nvfp4(h, status=None, stream=None) -> dict:
+    """NVFP4 quantisation of bf16 rows h [rows, d] on the device: codes [rows, d/2], packed block
+    scales and fp32 row scales [rows]."""
+    rows, d = int(h.shape[0]), int(h.shape[1])
+    dev = h.device
+    out = {"codes": torch.empty(rows, d // 2, dtype=torch.uint8, device=dev),
+           "block_scale": torch.empty(nvfp4_scale_bytes(rows, d), dtype=torch.uint8, device=dev),
+           "scale": torch.empty(rows, dtype=torch.float32, device=dev),
+           "status": torch.zeros(1, dtype=torch.int32, device=dev) if status is None else status}
+    _check(lib().dg_quantize_nvfp4(_ptr(h), rows, d, _ptr(out["codes"]), _ptr(out["block_scale"]),
+                                   _ptr(out["scale"]), _ptr(out["status"]), _stream(stream)),
+           "dg_quantize_nvfp4")
+    return out
+
+
 def dg_canvas_stats(h, w, *, B: int, S: int, h_scale=None, w_scale=None, inv_temp: float = 1.0,
-                    workspace=None, status=None, stream=None) -> dict:
+                    workspace=None, status=None, stream=None, **desc_kw) -> dict:
     """Per-slot argmax, confidence (max prob), entropy (nats) and per-canvas mean entropy."""
     dev = w.device
     R = B * S
-    desc = make_desc(h, w, B=B, S=S, h_scale=h_scale, w_scale=w_scale, inv_temp=inv_temp)
+    desc = make_desc(h, w, B=B, S=S, h_scale=h_scale, w_scale=w_scale, inv_temp=inv_temp, **desc_kw)
     ws = _workspace(desc, dev, workspace)
     out = {"argmax": torch.empty(R, dtype=torch.int32, device=dev),
            "conf": torch.empty(R, dtype=torch.float32, device=dev),
@@ -219,14 +265,14 @@ def dg_canvas_step(h, w, canvas_in, keep_k: int, seed: int, pass_: int, *, B: in
                    canvas_out=None, h_scale=None, w_scale=None, inv_temp: float = 1.0,
                    state=None, rule: StopRule | None = None, keep_rule: int = KEEP_CONFIDENCE,
                    mask_id: int | None = None, outputs: bool = True, workspace=None, status=None,
-                   stream=None) -> dict:
+                   stream=None, **desc_kw) -> dict:
     """One canvas pass: statistics, keep the top-K by confidence (or the K lowest-entropy slots
     with keep_rule=KEEP_ENTROPY), re-randomise the rest (or set them to mask_id)."""
     if rule is None and (keep_rule != KEEP_CONFIDENCE or mask_id is not None):
         rule = pass_rule(keep_rule, mask_id)
     dev = w.device
     R = B * S
-    desc = make_desc(h, w, B=B, S=S, h_scale=h_scale, w_scale=w_scale, inv_temp=inv_temp)
+    desc = make_desc(h, w, B=B, S=S, h_scale=h_scale, w_scale=w_scale, inv_temp=inv_temp, **desc_kw)
     ws = _workspace(desc, dev, workspace)
     out = {"canvas": canvas_out if canvas_out is not None else torch.empty(R, dtype=torch.int32, device=dev)}
     if outputs:

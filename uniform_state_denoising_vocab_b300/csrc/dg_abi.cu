@@ -60,7 +60,16 @@ HeadPlan plan_head_pair(int R, int V, int d, int max_pairs) {
 
 namespace {
 
-enum Path { PATH_SIMT = 0, PATH_TC_BF16 = 1, PATH_TC_E4M3 = 2, PATH_TC_E4M3_QUANT = 3 };
+enum Path {
+    PATH_SIMT = 0,
+    PATH_TC_BF16 = 1,
+    PATH_TC_E4M3 = 2,
+    PATH_TC_E4M3_QUANT = 3,  // bf16 h quantised to E4M3 on the device
+    PATH_FP4 = 4,            // NVFP4 h and w
+    PATH_FP4_QUANT = 5       // bf16 h quantised to NVFP4 on the device
+};
+
+inline bool quant_path(int path) { return path == PATH_TC_E4M3_QUANT || path == PATH_FP4_QUANT; }
 
 struct DeviceInfo {
     int sms = 0;
@@ -95,6 +104,9 @@ inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 int elem_size(int dt) { return dt == DG_F32 ? 4 : (dt == DG_BF16 ? 2 : 1); }
 
+// Bytes of one row of d elements of dtype dt (NVFP4 packs two elements per byte).
+long long row_bytes(int dt, long long d) { return dt == DG_NVFP4 ? d / 2 : d * elem_size(dt); }
+
 // Validates the descriptor; returns the execution path or a negative error.
 int classify(const dg_head_desc* d) {
     if (!d) return DG_ERR_INVALID_ARG;
@@ -112,12 +124,21 @@ int classify(const dg_head_desc* d) {
         path = PATH_TC_E4M3;
     else if (d->h_dtype == DG_BF16 && d->w_dtype == DG_E4M3)
         path = PATH_TC_E4M3_QUANT;
+    else if (d->h_dtype == DG_NVFP4 && d->w_dtype == DG_NVFP4)
+        path = PATH_FP4;
+    else if (d->h_dtype == DG_BF16 && d->w_dtype == DG_NVFP4)
+        path = PATH_FP4_QUANT;
     else
         return DG_ERR_UNSUPPORTED;
-    if (d->w_dtype == DG_E4M3 && !d->w_scale) return DG_ERR_INVALID_ARG;
-    if (d->h_dtype == DG_E4M3 && !d->h_scale) return DG_ERR_INVALID_ARG;
-    if ((static_cast<long long>(d->d) * elem_size(d->h_dtype)) % 16 != 0 ||
-        (static_cast<long long>(d->d) * elem_size(d->w_dtype)) % 16 != 0)
+    if ((d->w_dtype == DG_E4M3 || d->w_dtype == DG_NVFP4) && !d->w_scale) return DG_ERR_INVALID_ARG;
+    if ((d->h_dtype == DG_E4M3 || d->h_dtype == DG_NVFP4) && !d->h_scale) return DG_ERR_INVALID_ARG;
+    if (d->w_dtype == DG_NVFP4 && !d->w_block_scale) return DG_ERR_INVALID_ARG;
+    if (d->h_dtype == DG_NVFP4 && !d->h_block_scale) return DG_ERR_INVALID_ARG;
+    if (d->w_dtype == DG_NVFP4 && d->d % 256 != 0) return DG_ERR_UNSUPPORTED;
+    if (row_bytes(d->h_dtype, d->d) % 16 != 0 || row_bytes(d->w_dtype, d->d) % 16 != 0)
+        return DG_ERR_ALIGNMENT;
+    if ((d->h_block_scale && !aligned16(d->h_block_scale)) ||
+        (d->w_block_scale && !aligned16(d->w_block_scale)))
         return DG_ERR_ALIGNMENT;
     if ((d->h && !aligned16(d->h)) || !aligned16(d->w)) return DG_ERR_ALIGNMENT;
     if ((d->h_scale && !aligned16(d->h_scale)) || (d->w_scale && !aligned16(d->w_scale)))
@@ -127,13 +148,15 @@ int classify(const dg_head_desc* d) {
 
 struct Layout {
     HeadPlan plan;
-    size_t off_partials, off_ctl, off_stats, off_qh, off_sch, total;
+    size_t off_partials, off_ctl, off_stats, off_qh, off_sch, off_sfh, total;
 };
 
 int layout_for(const dg_head_desc* d, int path, const DeviceInfo& di, Layout* L) {
     const int R = d->B * d->S;
     if (path == PATH_SIMT)
         L->plan = plan_head(R, d->V, d->d, kSimtBM, kSimtBN, di.sms * 8);
+    else if (path == PATH_FP4 || path == PATH_FP4_QUANT)
+        L->plan = plan_head(R, d->V, d->d, kTcBM, kFp4BN, di.sms);  // single-CTA NVFP4 head
     else if (R > kTcBM && di.pairs > 0)
         L->plan = plan_head_pair(R, d->V, d->d, di.pairs);  // 256-row tiles over CTA pairs
     else
@@ -147,10 +170,17 @@ int layout_for(const dg_head_desc* d, int path, const DeviceInfo& di, Layout* L)
     off = up256(off + static_cast<size_t>(R) * 12);
     L->off_qh = off;
     L->off_sch = off;
+    L->off_sfh = off;
     if (path == PATH_TC_E4M3_QUANT) {
         off = up256(off + static_cast<size_t>(R) * d->d);
         L->off_sch = off;
         off = up256(off + static_cast<size_t>(R) * 4);
+    } else if (path == PATH_FP4_QUANT) {
+        off = up256(off + static_cast<size_t>(R) * (d->d / 2));
+        L->off_sch = off;
+        off = up256(off + static_cast<size_t>(R) * 4);
+        L->off_sfh = off;
+        off = up256(off + static_cast<size_t>(nvfp4_rows_pad(R)) * (d->d / 16));
     }
     L->total = off;
     return DG_OK;
@@ -185,6 +215,18 @@ thread_local cudaEvent_t t_prof_start = nullptr, t_prof_stop = nullptr;
 cudaError_t launch_head_only(const dg_head_desc* d, const Prepared& P, uint8_t* ws, uint32_t* status,
                              cudaStream_t stream);
 
+// a0: quantise bf16 h into the workspace for an E4M3 or NVFP4 head.
+cudaError_t launch_quantiser(const dg_head_desc* d, const Prepared& P, uint8_t* ws,
+                             uint32_t* status, cudaStream_t stream) {
+    const HeadPlan& pl = P.L.plan;
+    if (P.path == PATH_FP4_QUANT)
+        return launch_quant_rows_nvfp4(static_cast<const uint16_t*>(d->h), pl.R, pl.d,
+                                       ws + P.L.off_qh, ws + P.L.off_sfh,
+                                       reinterpret_cast<float*>(ws + P.L.off_sch), status, stream);
+    return launch_quant_rows(static_cast<const uint16_t*>(d->h), pl.R, pl.d, ws + P.L.off_qh,
+                             reinterpret_cast<float*>(ws + P.L.off_sch), status, stream);
+}
+
 // Enqueue a0 (if needed) and a1-a2 (head + partials) for the prepared descriptor, bracketing the
 // head kernel with the pending profiling events (outside graph capture only).
 cudaError_t enqueue_head(const dg_head_desc* d, const Prepared& P, uint8_t* ws, uint32_t* status,
@@ -200,16 +242,13 @@ cudaError_t enqueue_head(const dg_head_desc* d, const Prepared& P, uint8_t* ws, 
     }
     if (!e0) return launch_head_only(d, P, ws, status, stream);
     // a0 runs before the bracket so that the events time the head kernel alone
-    if (P.path == PATH_TC_E4M3_QUANT) {
-        const HeadPlan& pl = P.L.plan;
-        cudaError_t e = launch_quant_rows(static_cast<const uint16_t*>(d->h), pl.R, pl.d,
-                                          ws + P.L.off_qh, reinterpret_cast<float*>(ws + P.L.off_sch),
-                                          status, stream);
+    if (quant_path(P.path)) {
+        cudaError_t e = launch_quantiser(d, P, ws, status, stream);
         if (e != cudaSuccess) return e;
     }
     cudaEventRecord(e0, stream);
     Prepared Q = P;
-    if (Q.path == PATH_TC_E4M3_QUANT) Q.path = -PATH_TC_E4M3_QUANT;  // quantisation already done
+    if (quant_path(Q.path)) Q.path = -Q.path;  // quantisation already done
     cudaError_t e = launch_head_only(d, Q, ws, status, stream);
     cudaEventRecord(e1, stream);
     return e;
@@ -248,6 +287,20 @@ cudaError_t launch_head_only(const dg_head_desc* d, const Prepared& P, uint8_t* 
     case PATH_TC_E4M3:
         a.num_kb = (pl.d + 127) / 128;
         return launch_head_tc(1, d->h, d->w, a, pl, stream);
+    case PATH_FP4:
+        a.num_kb = pl.d / 256;
+        return launch_head_fp4(d->h, d->h_block_scale, d->w, d->w_block_scale, a, pl.grid, stream);
+    case PATH_FP4_QUANT:
+    case -PATH_FP4_QUANT: {
+        if (P.path > 0) {
+            e = launch_quantiser(d, P, ws, status, stream);
+            if (e != cudaSuccess) return e;
+        }
+        a.h_scale = reinterpret_cast<float*>(ws + P.L.off_sch);
+        a.num_kb = pl.d / 256;
+        return launch_head_fp4(ws + P.L.off_qh, ws + P.L.off_sfh, d->w, d->w_block_scale, a,
+                               pl.grid, stream);
+    }
     case PATH_TC_E4M3_QUANT:
     case -PATH_TC_E4M3_QUANT: {
         uint8_t* qh = ws + P.L.off_qh;
@@ -404,7 +457,7 @@ int dg_synth_denoise(void* user, const int32_t* canvas, const int32_t* pass, voi
     const dg_synth_params* sp = static_cast<const dg_synth_params*>(user);
     if (!sp || !sp->desc || !sp->y || !canvas || !pass || !h_out) return DG_ERR_INVALID_ARG;
     const dg_head_desc* d = sp->desc;
-    if (d->w_dtype == DG_F32 || d->h_dtype == DG_F32 || d->h_dtype == DG_E4M3)
+    if (d->w_dtype == DG_F32 || d->w_dtype == DG_NVFP4 || d->h_dtype != DG_BF16)
         return DG_ERR_UNSUPPORTED;  // writes bf16 hidden states from a bf16 or e4m3 head
     if (launch_synth_denoise(d, sp->y, sp->n_content, sp->s_content, sp->s_pad, canvas, pass,
                              static_cast<uint16_t*>(h_out), sp->status,
@@ -471,6 +524,8 @@ void copy_desc(dg_head_desc* dst, const dg_head_desc& s) {
     dst->w = s.w;
     dst->w_scale = s.w_scale;
     dst->inv_temp = s.inv_temp;
+    dst->h_block_scale = s.h_block_scale;
+    dst->w_block_scale = s.w_block_scale;
 }
 
 void copy_params(dg_loop_params* dst, const dg_loop_params& s) {
@@ -668,7 +723,9 @@ extern "C" int dg_canvas_loop(const dg_head_desc* desc, int32_t* canvas, void* h
         const dg_synth_params* sp = static_cast<const dg_synth_params*>(user);
         if (!sp || !sp->desc || !sp->y) return DG_ERR_INVALID_ARG;
         // the built-in denoiser writes bf16 hidden states from a bf16 or E4M3 head
-        if (sp->desc->w_dtype == DG_F32 || desc->h_dtype != DG_BF16) return DG_ERR_UNSUPPORTED;
+        if (sp->desc->w_dtype == DG_F32 || sp->desc->w_dtype == DG_NVFP4 ||
+            desc->h_dtype != DG_BF16)
+            return DG_ERR_UNSUPPORTED;
     }
 
     LoopKey key;
@@ -781,5 +838,35 @@ extern "C" int dg_block_generate(const dg_head_desc* desc, int32_t n_blocks,
                             cudaMemcpyDeviceToDevice, st) != cudaSuccess)
             return DG_ERR_CUDA;
     }
+    return DG_OK;
+}
+
+extern "C" int dg_nvfp4_scale_bytes(int32_t rows, int32_t d, size_t* bytes) {
+    if (!bytes || rows < 1 || d < 64 || d % 64 != 0) return DG_ERR_INVALID_ARG;
+    *bytes = static_cast<size_t>(dg::nvfp4_rows_pad(rows)) * (d / 16);
+    return DG_OK;
+}
+
+extern "C" int dg_nvfp4_pack_scales(const uint8_t* block_scales, int32_t rows, int32_t d,
+                                    uint8_t* packed, dg_stream_t stream) {
+    if (!block_scales || !packed || rows < 1 || d < 64 || d % 64 != 0) return DG_ERR_INVALID_ARG;
+    if (dg::launch_pack_scales(block_scales, rows, d, packed,
+                               reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return DG_ERR_CUDA;
+    return DG_OK;
+}
+
+extern "C" int dg_quantize_nvfp4(const void* h_bf16, int32_t rows, int32_t d, uint8_t* codes,
+                                 uint8_t* block_scale_packed, float* row_scale, uint32_t* status,
+                                 dg_stream_t stream) {
+    if (!h_bf16 || !codes || !block_scale_packed || !row_scale || rows < 1 || d < 64 ||
+        d % 64 != 0)
+        return DG_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(h_bf16) & 15u) || (reinterpret_cast<uintptr_t>(codes) & 7u))
+        return DG_ERR_ALIGNMENT;
+    if (dg::launch_quant_rows_nvfp4(static_cast<const uint16_t*>(h_bf16), rows, d, codes,
+                                    block_scale_packed, row_scale, status,
+                                    reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return DG_ERR_CUDA;
     return DG_OK;
 }

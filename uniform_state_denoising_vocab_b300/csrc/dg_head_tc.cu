@@ -266,6 +266,11 @@ bool make_map(CUtensorMap* m, const void* base, int elem_bytes, int rows, int co
 
 }  // namespace
 
+// Row-major [rows, cols_bytes] byte matrix, box 128 bytes x box_rows, 128-byte swizzle.
+bool make_map_u8(CUtensorMap* m, const void* base, int rows, int cols_bytes, int box_rows) {
+    return make_map(m, base, 1, rows, cols_bytes, box_rows);
+}
+
 cudaError_t launch_head_tc(int kind, const void* h, const void* w, const HeadArgs& args,
                            const HeadPlan& plan, cudaStream_t stream) {
     const int eb = kind == 0 ? 2 : 1;

@@ -16,6 +16,13 @@ constexpr int kTcBN = 256;
 constexpr int kTcStages = 4;
 constexpr int kTc2Stages = 6;    // pair kernel: 32 KB stages (128 h rows + 128 W rows)
 constexpr int kTcThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+// NVFP4 head: vocabulary rows per tile, accumulator buffers and pipeline stages. TMEM holds
+// kFp4Acc accumulators of kFp4BN columns plus the scale factors of every stage in flight; of the
+// configurations that fit, 256-row tiles with one accumulator and 4 stages measured fastest (128-row
+// tiles with two accumulators re-read h twice as often and issue more scale copies per column).
+constexpr int kFp4BN = 256;
+constexpr int kFp4Acc = 1;
+constexpr int kFp4Stages = 4;
 // Geometry of the fp32 CUDA-core head.
 constexpr int kSimtBM = 128;
 constexpr int kSimtBN = 64;
@@ -102,6 +109,15 @@ cudaError_t launch_head_tc2(int kind, const CUtensorMap& ma, const CUtensorMap& 
                             const HeadArgs& args, int n_pairs, cudaStream_t stream);
 // Resident clusters of the pair kernel on the current device (0 if it cannot run).
 int head_tc2_max_pairs();
+// NVFP4 head (single-CTA, block-scaled MMAs): codes + packed block scales of h and w.
+cudaError_t launch_head_fp4(const void* qh, const uint8_t* sfa, const void* qw, const uint8_t* sfb,
+                            const HeadArgs& args, int grid, cudaStream_t stream);
+// NVFP4 preparation (dg_nvfp4.cu). Packed block-scale arrays cover nvfp4_rows_pad(rows) rows.
+int nvfp4_rows_pad(int rows);
+cudaError_t launch_quant_rows_nvfp4(const uint16_t* h, int R, int d, uint8_t* q, uint8_t* sf,
+                                    float* scale, uint32_t* status, cudaStream_t stream);
+cudaError_t launch_pack_scales(const uint8_t* plain, int rows, int d, uint8_t* packed,
+                               cudaStream_t stream);
 // fp32 CUDA-core head.
 cudaError_t launch_head_simt(const float* h, const float* w, const HeadArgs& args, int grid,
                              cudaStream_t stream);

@@ -294,3 +294,61 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask
 }
 
 }  // namespace dg
+
+// ---------------------------------------------------------------------------------------------
+// Block-scaled FP4 (NVFP4) pieces: bulk copies of scale-factor atoms, the scale-factor copy into
+// tensor memory and the block-scaled MMA (single-CTA group).
+// ---------------------------------------------------------------------------------------------
+namespace dg {
+
+// Contiguous global -> shared copy of `bytes` (multiple of 16, both addresses 16-byte aligned),
+// completion counted on an mbarrier of this CTA.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(gmem_src)), "r"(bytes),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Shared-memory descriptor of a 32-row x 16-byte matrix stored row-major without swizzle
+// (four 8-row core matrices 128 bytes apart): the source of a 32x128b tensor-memory copy.
+__device__ __forceinline__ uint64_t sdesc_rows16_noswizzle(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(128 >> 4) << 16;   // leading byte offset (one core matrix along K)
+    d |= static_cast<uint64_t>(128 >> 4) << 32;   // stride byte offset: next 8 rows
+    d |= static_cast<uint64_t>(1) << 46;          // descriptor version
+    return d;                                      // swizzle mode 0 (none)
+}
+
+// Copy 32 lanes x 128 bits from shared memory into tensor memory at `taddr`, replicated into the
+// four lane quadrants (each warp's 32 lanes see the same 4 columns).
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+
+// Instruction descriptor of a block-scaled E2M1 x E2M1 MMA with fp32 accumulation and UE4M3
+// scale factors, A and B K-major, shape M x N:
+//   bits 7-9 / 10-12 A/B format (E2M1 = 1 for the MX FP4 kinds), 15/16 majors (0 = K),
+//   17-22 N >> 3, 23 scale format (0 = UE4M3), 24-28 M >> 4; scale-factor ids 0.
+__host__ __device__ constexpr uint32_t idesc_nvfp4(uint32_t M, uint32_t N) {
+    return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// D (+)= A x B with per-16-element UE4M3 scale factors of A and B read from tensor memory.
+__device__ __forceinline__ void mma_nvfp4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, "
+        "[%5], [%6], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+
+}  // namespace dg

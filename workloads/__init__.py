@@ -12,5 +12,6 @@ from .gen import (  # noqa: F401
     make_loop_inputs,
     normal_f32,
     quantize_rows_e4m3_bits,
+    quantize_rows_nvfp4_bits,
     uniform_ints,
 )

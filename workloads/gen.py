@@ -98,11 +98,58 @@ def quantize_rows_e4m3_bits(w_bf16: np.ndarray, rows: int, d: int) -> tuple[np.n
     return q, sc
 
 
+_E2M1_THRESHOLDS = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+
+
+def quantize_rows_nvfp4_bits(w_bf16: np.ndarray, rows: int, d: int):
+    """NVFP4 quantisation of a bf16 weight matrix (how a 4-bit checkpoint stores the head), in
+    float32: g = amax_row / 2688; per block of 16 elements sb = E4M3(bmax / (6 g)) (torch cast,
+    nearest-even); codes = E2M1 nearest-even of w / (sb g), saturating at 6 (0 where sb = 0).
+
+    Returns (codes packed two per byte, element 2j in the low nibble [rows*d/2], plain E4M3 block
+    scales [rows*d/16], float32 row scales [rows]). Chunked over rows to bound memory.
+    """
+    assert d % 16 == 0
+    q = np.empty(rows * d // 2, dtype=np.uint8)
+    bs = np.empty(rows * d // 16, dtype=np.uint8)
+    sc = np.empty(rows, dtype=np.float32)
+    step = max(1, (1 << 22) // d)
+    src = np.asarray(w_bf16, dtype=np.uint16)
+    for r0 in range(0, rows, step):
+        r1 = min(rows, r0 + step)
+        x = (src[r0 * d:r1 * d].astype(np.uint32) << 16).view(np.float32).reshape(r1 - r0, d)
+        ax = np.abs(x)
+        amax = ax.max(axis=1)
+        zero = amax == 0
+        g = np.where(zero, np.float32(1), amax / np.float32(2688)).astype(np.float32)
+        g6 = (np.float32(6) * g).astype(np.float32)
+        bmax = ax.reshape(r1 - r0, d // 16, 16).max(axis=2)
+        t = (bmax / g6[:, None]).astype(np.float32)
+        sbt = torch.from_numpy(t).to(torch.float8_e4m3fn)
+        sb = sbt.view(torch.uint8).numpy()
+        sb[zero] = 0
+        sv = sbt.float().numpy()
+        sv[zero] = 0
+        db = (sv * g[:, None]).astype(np.float32)
+        safe = np.where(db > 0, db, np.float32(1))
+        y = (x.reshape(r1 - r0, d // 16, 16) / safe[:, :, None]).astype(np.float32)
+        a = np.abs(y)
+        idx = np.searchsorted(_E2M1_THRESHOLDS, a, side="left")
+        tie = (idx < 7) & (a == _E2M1_THRESHOLDS[np.minimum(idx, 6)]) & (idx % 2 == 1)
+        code = (idx + tie).astype(np.uint8) | np.where(np.signbit(y), 8, 0).astype(np.uint8)
+        code[db == 0] = 0
+        code = code.reshape(r1 - r0, d)
+        q[r0 * d // 2:r1 * d // 2] = (code[:, 0::2] | (code[:, 1::2] << 4)).reshape(-1)
+        bs[r0 * d // 16:r1 * d // 16] = sb.reshape(-1)
+        sc[r0:r1] = g
+    return q, bs, sc
+
+
 @dataclass(frozen=True)
 class WorkloadConfig:
     """One synthetic workload: B canvases of S slots, hidden size d, vocabulary V."""
     name: str
-    precision: str          # "f32" | "bf16" | "e4m3"
+    precision: str          # "f32" | "bf16" | "e4m3" | "nvfp4"
     B: int
     S: int
     V: int
@@ -136,6 +183,9 @@ CONFIGS: dict[str, WorkloadConfig] = {
     "pass_bf16_b8_v262144_d2816": WorkloadConfig(
         "pass_bf16_b8_v262144_d2816", "bf16", 8, 256, 262144, 2816, seed=2, mode="pass",
         note="8 independent canvases (2048 rows), bf16 head"),
+    "pass_nvfp4_v262144_d2816": WorkloadConfig(
+        "pass_nvfp4_v262144_d2816", "nvfp4", 1, 256, 262144, 2816, seed=4, mode="pass",
+        note="single canvas pass, NVFP4 head (E2M1 + per-16 E4M3 block scales + row scale)"),
     "loop_e4m3_v262144_d2816": WorkloadConfig(
         "loop_e4m3_v262144_d2816", "e4m3", 1, 256, 262144, 2816, seed=3, mode="loop",
         note="full denoise loop, FP8-E4M3 head with per-row fp32 scales"),
@@ -157,6 +207,9 @@ def make_head(cfg: WorkloadConfig, V: int | None = None, d: int | None = None):
     del w
     if cfg.precision == "bf16":
         return {"w": wb, "w_scale": None}
+    if cfg.precision == "nvfp4":
+        q, bs, sc = quantize_rows_nvfp4_bits(wb, V, d)
+        return {"w": q, "w_scale": sc, "w_bscale": bs}
     q, sc = quantize_rows_e4m3_bits(wb, V, d)
     return {"w": q, "w_scale": sc, "w_bf16": wb}
 
