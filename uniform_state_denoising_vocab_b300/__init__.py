@@ -117,8 +117,9 @@ def lib():
 
 def dg_profile_next_head(start: torch.cuda.Event, stop: torch.cuda.Event) -> None:
     """Bracket the next head kernel launched by this thread with two recorded CUDA events."""
-    start.record()   # materialise the underlying cudaEvent_t handles
-    stop.record()
+    for ev in (start, stop):
+        if not ev.cuda_event:   # torch creates the cudaEvent_t lazily, at its first record
+            ev.record()
     _check(lib().dg_profile_next_head(C.c_void_p(start.cuda_event), C.c_void_p(stop.cuda_event)),
            "dg_profile_next_head")
 
