@@ -78,6 +78,9 @@ __global__ void __cluster_dims__(kMergeCluster, 1, 1) __maxnreg__(40)
     merge_select_kernel(const SelectArgs a) {
     __shared__ MergeSmem sm;
     grid_dependency_wait();
+    // the next pass's first kernel may be scheduled now and run its prologue beside this grid;
+    // it waits for this grid's completion before touching the canvas or the statistics
+    grid_launch_dependents();
     if (a.ctl != nullptr && *reinterpret_cast<const volatile int32_t*>(&a.ctl->stop) != 0)
         return;  // the loop ended in an earlier pass of this graph iteration (uniform)
     const int b = blockIdx.x / kMergeCluster;
