@@ -1,4 +1,7 @@
-// dg_internal.h -- host-side launch interfaces between the C ABI (dg_abi.cu) and the kernels.
+// dg_internal.h -- what the C ABI (dg_abi.cu) and the kernel files share: tile geometry, the head
+// work plan, the argument blocks of each launch, the launch functions, and the small device helpers
+// every kernel of a pass uses (programmatic dependent launch, the per-pass timeline, the pass's
+// temperature).
 #pragma once
 #include <cstddef>
 #include <cstdint>
@@ -183,8 +186,9 @@ cudaError_t launch_loop_init(int32_t* canvas, int R, int S, int B, int V, uint64
 cudaError_t launch_trace_copy(const void* src, void* dst, size_t bytes, const LoopCtl* ctl,
                               cudaStream_t stream);
 
-// Built-in synthetic denoiser (stop: optional loop stop flag, non-zero = do nothing). With q_out/scale_out non-null it also quantises each bf16 row
-// it writes to E4M3 with the per-row absmax rule of launch_quant_rows (one kernel instead of two).
+// Built-in synthetic denoiser (stop: optional loop stop flag, non-zero = do nothing). With
+// q_out/scale_out non-null it also quantises each bf16 row it writes to E4M3 with the per-row
+// absmax rule of launch_quant_rows (one kernel instead of two).
 cudaError_t launch_synth_denoise(const dg_head_desc* desc, const int32_t* y, int n_content,
                                  float s_content, float s_pad, const int32_t* canvas,
                                  const int32_t* pass, uint16_t* h_out, uint32_t* status,
