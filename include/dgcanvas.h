@@ -277,15 +277,17 @@ DG_API int dg_block_generate(const dg_head_desc* desc, int32_t n_blocks, const i
  *   dg_nvfp4_scale_bytes: size of the packed block-scale array of `rows` rows of width d:
  *     ceil(rows / 256) * 256 * d / 16 bytes.
  *   dg_nvfp4_pack_scales: block scales [rows, d/16] (row-major, E4M3) -> the packed layout the
- *     block-scaled MMA consumes: one 512-byte atom per (128-row group g, 64-element step j) at
- *     offset (g * d/64 + j) * 512, byte (m % 32) * 16 + (m / 32) * 4 + kb holding row 128 g + m,
- *     block 4 j + kb; rows past `rows` are zero. Device pointers, d % 64 == 0.
+ *     block-scaled MMA consumes: one 4096-byte chunk per (256-row group G, 256-element K slice s)
+ *     at offset (G * d/256 + s) * 4096; the scale of row 256 G + m (l = m % 32, c = m / 32),
+ *     block 16 s + 4 j + kb sits at byte
+ *       (l / 8) * 1024 + j * 256 + (c / 4) * 128 + (l % 8) * 16 + (c % 4) * 4 + kb
+ *     of its chunk; rows past `rows` are zero. Device pointers, d % 256 == 0.
  *   dg_quantize_nvfp4: two-level NVFP4 quantisation of bf16 rows [rows, d] on the device, in
  *     IEEE binary32: amax = max |h|; amax == 0 gives row scale 1 and zero codes / block scales;
  *     else g = amax / 2688, per block of 16: sb = e4m3_rn_satfinite(bmax / (6 g)), codes
  *     q = e2m1_rn_satfinite(h / (value(sb) g)) (0 where sb = 0). Writes codes [rows, d/2], packed
  *     block scales (dg_nvfp4_scale_bytes) and row scales [rows]. Sets DG_ST_NONFINITE on
- *     non-finite input. d % 64 == 0.
+ *     non-finite input. d % 256 == 0.
  */
 DG_API int dg_nvfp4_scale_bytes(int32_t rows, int32_t d, size_t* bytes);
 DG_API int dg_nvfp4_pack_scales(const uint8_t* block_scales, int32_t rows, int32_t d,

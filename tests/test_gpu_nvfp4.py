@@ -24,12 +24,17 @@ def _bits(x):
 
 
 def _unpack_scales(packed, rows, d):
-    """Invert the documented packed layout: atom (g, j) at (g * d/64 + j) * 512, byte
-    (m % 32) * 16 + (m / 32) * 4 + kb for row 128 g + m, block 4 j + kb."""
-    nb, nks = d // 16, d // 64
+    """Invert the documented packed layout: chunk (G, s) at (G * d/256 + s) * 4096; row 256 G + m
+    (l = m % 32, c = m / 32), block 16 s + 4 j + kb at byte
+    (l / 8) * 1024 + j * 256 + (c / 4) * 128 + (l % 8) * 16 + (c % 4) * 4 + kb of the chunk."""
+    nb, nsl = d // 16, d // 256
     r = np.arange(rows)[:, None]
     b = np.arange(nb)[None, :]
-    off = ((r // 128) * nks + b // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + b % 4
+    G, m = r // 256, r % 256
+    l, c = m % 32, m // 32
+    s, j, kb = b // 16, (b // 4) % 4, b % 4
+    off = ((G * nsl + s) * 4096 + (l // 8) * 1024 + j * 256 + (c // 4) * 128 + (l % 8) * 16 +
+           (c % 4) * 4 + kb)
     return np.asarray(packed)[off]
 
 

@@ -30,6 +30,7 @@ HeadPlan plan_head(int R, int V, int d, int BM, int BN, int slots) {
     p.units = p.MB * g;
     p.grid = p.units < slots ? p.units : slots;
     p.pair = 0;
+    p.parts = 1;
     return p;
 }
 
@@ -55,6 +56,7 @@ HeadPlan plan_head_pair(int R, int V, int d, int max_pairs) {
     p.units = p.MB * g;
     p.grid = p.units < max_pairs ? p.units : max_pairs;
     p.pair = 1;
+    p.parts = 1;
     return p;
 }
 
@@ -155,15 +157,17 @@ int layout_for(const dg_head_desc* d, int path, const DeviceInfo& di, Layout* L)
     const int R = d->B * d->S;
     if (path == PATH_SIMT)
         L->plan = plan_head(R, d->V, d->d, kSimtBM, kSimtBN, di.sms * 8);
-    else if (path == PATH_FP4 || path == PATH_FP4_QUANT)
+    else if (path == PATH_FP4 || path == PATH_FP4_QUANT) {
         L->plan = plan_head(R, d->V, d->d, kTcBM, kFp4BN, di.sms);  // single-CTA NVFP4 head
+        L->plan.parts = 2;  // its epilogue keeps one state per half of the tile's columns
+    }
     else if (R > kTcBM && di.pairs > 0)
         L->plan = plan_head_pair(R, d->V, d->d, di.pairs);  // 256-row tiles over CTA pairs
     else
         L->plan = plan_head(R, d->V, d->d, kTcBM, kTcBN, di.sms);
     size_t off = 0;
     L->off_partials = off;
-    off = up256(off + static_cast<size_t>(L->plan.n_groups) * R * 16);
+    off = up256(off + static_cast<size_t>(L->plan.n_groups) * L->plan.parts * R * 16);
     L->off_ctl = off;
     off = up256(off + sizeof(LoopCtl));
     L->off_stats = off;  // argmax, conf, entropy [R] each, for outputs the caller leaves NULL
@@ -321,7 +325,7 @@ cudaError_t launch_head_only(const dg_head_desc* d, const Prepared& P, uint8_t* 
 SelectArgs base_select(const dg_head_desc* d, const Prepared& P, uint8_t* ws, uint32_t* status) {
     SelectArgs s{};
     s.partials = reinterpret_cast<const float4*>(ws + P.L.off_partials);
-    s.n_groups = P.L.plan.n_groups;
+    s.n_groups = P.L.plan.n_groups * P.L.plan.parts;  // partials per row
     s.R = d->B * d->S;
     s.S = d->S;
     s.B = d->B;
@@ -842,14 +846,15 @@ extern "C" int dg_block_generate(const dg_head_desc* desc, int32_t n_blocks,
 }
 
 extern "C" int dg_nvfp4_scale_bytes(int32_t rows, int32_t d, size_t* bytes) {
-    if (!bytes || rows < 1 || d < 64 || d % 64 != 0) return DG_ERR_INVALID_ARG;
+    if (!bytes || rows < 1 || d < 256 || d % 256 != 0) return DG_ERR_INVALID_ARG;
     *bytes = static_cast<size_t>(dg::nvfp4_rows_pad(rows)) * (d / 16);
     return DG_OK;
 }
 
 extern "C" int dg_nvfp4_pack_scales(const uint8_t* block_scales, int32_t rows, int32_t d,
                                     uint8_t* packed, dg_stream_t stream) {
-    if (!block_scales || !packed || rows < 1 || d < 64 || d % 64 != 0) return DG_ERR_INVALID_ARG;
+    if (!block_scales || !packed || rows < 1 || d < 256 || d % 256 != 0)
+        return DG_ERR_INVALID_ARG;
     if (dg::launch_pack_scales(block_scales, rows, d, packed,
                                reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return DG_ERR_CUDA;
@@ -859,8 +864,8 @@ extern "C" int dg_nvfp4_pack_scales(const uint8_t* block_scales, int32_t rows, i
 extern "C" int dg_quantize_nvfp4(const void* h_bf16, int32_t rows, int32_t d, uint8_t* codes,
                                  uint8_t* block_scale_packed, float* row_scale, uint32_t* status,
                                  dg_stream_t stream) {
-    if (!h_bf16 || !codes || !block_scale_packed || !row_scale || rows < 1 || d < 64 ||
-        d % 64 != 0)
+    if (!h_bf16 || !codes || !block_scale_packed || !row_scale || rows < 1 || d < 256 ||
+        d % 256 != 0)
         return DG_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(h_bf16) & 15u) || (reinterpret_cast<uintptr_t>(codes) & 7u))
         return DG_ERR_ALIGNMENT;

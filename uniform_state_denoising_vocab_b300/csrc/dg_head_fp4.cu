@@ -10,23 +10,29 @@
 //
 // Operand layouts (device, prepared by dg_quantize_nvfp4 / dg_nvfp4_pack_scales):
 //   codes: [rows][d/2] bytes, element 2j in the low nibble of byte j;
-//   block scales: one 512-byte atom per (128-row group, 64-element K step): byte
-//     (m % 32) * 16 + (m / 32) * 4 + kb holds the scale of row 128 g + m, K block 4 j + kb, which
-//     a 32x128b tensor-memory copy places at lane m % 32, column m / 32 (replicated over the four
-//     lane quadrants): the scale-factor layout the block-scaled MMA reads.
+//   block scales: one 4096-byte chunk per (256-row group, 256-element K slice), in the order the
+//     tensor-memory copies read (layout in dg_nvfp4.cu). The block-scaled MMA reads the scale of
+//     tile row m (lane quadrant q = m / 32) for a 64-element step from TMEM lane m, column
+//     (scale column + q); the scales of the 256 w rows of a step occupy 8 columns of every lane
+//     quadrant.
 //
-// Structure (one CTA of 192 threads per SM; 128 x 256 tiles; K slices of 256 elements):
-//   warp 0     TMA loads of the A / B code slices (128-byte swizzle) and bulk loads of their
-//              scale atoms into a 4-stage ring;
+// Structure (one CTA of 320 threads per SM; 128 x 256 tiles; K slices of 256 elements):
+//   warp 0     TMA loads of the A / B code slices (128-byte swizzle) and bulk loads of the scale
+//              chunks into a 3-stage ring: the h chunk once, the w chunk four times (one copy
+//              per lane quadrant, so that a single 128x256b copy fills all four);
 //   warp 1     owns 512 TMEM columns: the accumulator and one set of scale-factor columns per
-//              stage; one thread copies each stage's scale atoms into tensor memory (tcgen05.cp,
-//              12 copies of 512 bytes) and issues 4 block-scaled MMAs (M=128, N=256, K=64);
-//   warps 2-5  epilogue as in the other heads (one slot row per thread).
+//              stage; one thread copies each stage's scales into tensor memory (per 64-element
+//              step: a 32x128b copy of the h row block's half, replicated over the lane quadrants,
+//              and a 128x256b copy of the w scales) and issues 4 block-scaled MMAs (M=128, N=256,
+//              K=64);
+//   warps 2-9  epilogue: two warps per lane quadrant (one slot row per thread), each folding one
+//              half of the tile's 256 columns into its own running state, so a unit writes two
+//              partials per row.
 // The scale factors of every stage in flight share the 512 TMEM columns with the accumulator, so
 // a 256-column tile has a single accumulator and its epilogue does not overlap the next tile's
-// MMAs. Measured on the 256 x 262144 x 2816 head: 156 us per launch, of which removing the scale
-// copies saves ~55 us (each copy costs ~30 ns in the tensor pipe's issue order) and removing the
-// epilogue ~40 us; both are the known limits of this kernel.
+// MMAs. Scale copies are issued in order with the MMAs and cost about the same per instruction
+// whatever their size, which is why the w scales travel as one 128x256b copy per step rather than
+// two replicated 32x128b copies.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -39,21 +45,22 @@ namespace dg {
 namespace {
 
 constexpr int BM = 128, BN = kFp4BN, NACC = kFp4Acc, STAGES = kFp4Stages;
-constexpr int KSLICE = 256;                      // FP4 elements per 128-byte K slice
-constexpr int KSTEP = 64;                        // elements per MMA
 constexpr int A_BYTES = BM * 128;
 constexpr int B_BYTES = BN * 128;
-constexpr int SF_ATOM = 512;
-constexpr int BGROUPS = BN / 128;                // 128-row scale groups per B tile
-constexpr int SFA_BYTES = 4 * SF_ATOM;           // 4 K steps x one 128-row group
-constexpr int SFB_BYTES = BGROUPS * 4 * SF_ATOM; // groups x 4 K steps
+constexpr int SF_CHUNK = 4096;                   // packed scales of 256 rows x one K slice
+constexpr int SFA_BYTES = SF_CHUNK;              // the chunk holding this row block's scales
+constexpr int SFB_BYTES = 4 * SF_CHUNK;          // the w chunk once per TMEM lane quadrant
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+constexpr int EPI_WARPS = kFp4Threads / 32 - 2;  // two per lane quadrant
+constexpr int HALF = BN / 2;                     // columns per epilogue warp
+static_assert(BN == 256, "a w scale chunk covers 256 vocabulary rows");
+static_assert(EPI_WARPS == 8, "two epilogue warps per lane quadrant");
 constexpr int TMEM_COLS = 512;
 constexpr uint32_t SF_COL0 = NACC * BN;          // scale-factor columns after the accumulators
 constexpr uint32_t SFB_COLS = BN / 32;           // scale columns of B per MMA
 constexpr uint32_t SF_COLS_PER_STAGE = 4 * 4 + 4 * SFB_COLS;
 static_assert(SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 4 * BN * 4 + 256;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_WARPS * HALF * 4 + 256;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 struct SmemCtl {
@@ -69,7 +76,7 @@ __device__ __forceinline__ void set_abort(SmemCtl* c, uint32_t* status) {
     flag_status(status, DG_ST_TIMEOUT);
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kFp4Threads, 1)
     head_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const HeadArgs args, const uint8_t* __restrict__ sfa_g,
                     const uint8_t* __restrict__ sfb_g) {
@@ -81,12 +88,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t* sSFA = sB + STAGES * B_BYTES;
     uint8_t* sSFB = sSFA + STAGES * SFA_BYTES;
     float* s_csc = reinterpret_cast<float*>(sSFB + STAGES * SFB_BYTES);
-    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(s_csc + 4 * BN);
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(s_csc + EPI_WARPS * HALF);
     const volatile int* abort_flag = &ctl->abort;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int nks = args.num_kb * (KSLICE / KSTEP);  // 64-element K steps per row
+    const int nsl = args.num_kb;  // 256-element K slices per row (one scale chunk each)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
@@ -95,7 +102,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int i = 0; i < NACC; ++i) {
             mbar_init(&ctl->tfull[i], 1);
-            mbar_init(&ctl->tempty[i], 4);
+            mbar_init(&ctl->tempty[i], EPI_WARPS);
         }
         mbar_init(&ctl->drain, 1);
         ctl->abort = 0;
@@ -139,15 +146,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                     &ctl->full[stage], pol_h);
                         tma_load_2d(sB + stage * B_BYTES, &tmB, kb * 128, nb * BN,
                                     &ctl->full[stage], pol_w);
-                        // scale atoms of the slice: K steps 4 kb .. 4 kb + 3 are contiguous
+                        // scale chunks of the slice: the h chunk once, the w chunk per quadrant
                         bulk_load(sSFA + stage * SFA_BYTES,
-                                  sfa_g + (static_cast<size_t>(mb) * nks + 4 * kb) * SF_ATOM,
-                                  SFA_BYTES, &ctl->full[stage]);
-                        for (int g = 0; g < BGROUPS; ++g)
-                            bulk_load(sSFB + stage * SFB_BYTES + g * 4 * SF_ATOM,
-                                      sfb_g + (static_cast<size_t>(BGROUPS * nb + g) * nks + 4 * kb) *
-                                                  SF_ATOM,
-                                      4 * SF_ATOM, &ctl->full[stage]);
+                                  sfa_g + (static_cast<size_t>(mb >> 1) * nsl + kb) * SF_CHUNK,
+                                  SF_CHUNK, &ctl->full[stage]);
+                        const uint8_t* wchunk =
+                            sfb_g + (static_cast<size_t>(nb) * nsl + kb) * SF_CHUNK;
+                        for (int q = 0; q < 4; ++q)
+                            bulk_load(sSFB + stage * SFB_BYTES + q * SF_CHUNK, wchunk, SF_CHUNK,
+                                      &ctl->full[stage]);
                         parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
                         ++issued;
                         if (++stage == STAGES) {
@@ -172,6 +179,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool ok = true;
             for (int unit = blockIdx.x; unit < units && ok; unit += gridDim.x) {
                 const int grp = unit / args.MB;
+                const uint32_t a_half = ((unit % args.MB) & 1) * 128;  // row block's half of the chunk
                 for (int nb = grp; nb < args.NT && ok; nb += args.n_groups, ++tcount) {
                     const uint32_t buf = tcount % NACC, tph = (tcount / NACC) & 1u;
                     if (!mbar_wait(&ctl->tempty[buf], tph ^ 1u, abort_flag)) {
@@ -191,14 +199,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const uint32_t sf_col = tmem_base + SF_COL0 + stage * SF_COLS_PER_STAGE;
                         const uint32_t sa = smem_u32(sSFA + stage * SFA_BYTES);
                         const uint32_t sb = smem_u32(sSFB + stage * SFB_BYTES);
+                        // step j: h scales from byte j * 256 + a_half of the chunk (8-row
+                        // groups 1024 bytes apart), replicated over the lane quadrants; w scales
+                        // from byte j * 256 of the four chunk copies (quadrant q's rows 4096 q on)
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            tmem_cp_32x128b_x4(sf_col + 4 * j, sdesc_rows16_noswizzle(sa + j * SF_ATOM));
-#pragma unroll
-                            for (int g = 0; g < BGROUPS; ++g)
-                                tmem_cp_32x128b_x4(
-                                    sf_col + 16 + SFB_COLS * j + 4 * g,
-                                    sdesc_rows16_noswizzle(sb + (g * 4 + j) * SF_ATOM));
+                            tmem_cp_32x128b_x4(sf_col + 4 * j,
+                                               sdesc_noswizzle(sa + j * 256 + a_half, 1024, 1024));
+                            tmem_cp_128x256b(sf_col + 16 + SFB_COLS * j,
+                                             sdesc_noswizzle(sb + j * 256, 128, 1024));
                         }
                         const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sA + stage * A_BYTES));
                         const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sB + stage * B_BYTES));
@@ -220,9 +229,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else {
         // ---------------------------------------------------------------- epilogue
-        const int quad = warp & 3;
+        const int ew = warp - 2;
+        const int quad = warp & 3;       // TMEM lane quadrant this warp may access
+        const int half = ew >> 2;        // columns [half * HALF, half * HALF + HALF) of each tile
         const int row_in_block = quad * 32 + lane;
-        float* csc = s_csc + (warp - 2) * BN;
+        const int parts_per_row = 2 * args.n_groups;
+        float* csc = s_csc + ew * HALF;
         uint32_t tcount = 0;
         bool ok = true;
         for (int unit = blockIdx.x; unit < units && ok; unit += gridDim.x) {
@@ -233,8 +245,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             RowState st = row_state_init();
             for (int nb = grp; nb < args.NT && ok; nb += args.n_groups, ++tcount) {
                 const uint32_t buf = tcount % NACC, tph = (tcount / NACC) & 1u;
-                const int n_base = nb * BN;
-                stage_column_scales<BN>(csc, args.w_scale, n_base, args.V, lane);
+                const int n_base = nb * BN + half * HALF;
+                stage_column_scales<HALF>(csc, args.w_scale, n_base, args.V, lane);
                 if (!mbar_wait(&ctl->tfull[buf], tph, abort_flag)) {
                     set_abort(ctl, args.status);
                     ok = false;
@@ -242,14 +254,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t taddr0 =
-                    tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * BN;
-                drain_tile<1, BN>(st, taddr0, csc, crow, n_base, args.V - n_base);
+                    tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * BN + half * HALF;
+                drain_tile<1, HALF>(st, taddr0, csc, crow, n_base, args.V - n_base);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
             }
             if (ok && row < args.R)
-                args.partials[static_cast<size_t>(row) * args.n_groups + grp] =
+                args.partials[static_cast<size_t>(row) * parts_per_row + 2 * grp + half] =
                     pack(row_state_partial(st));
         }
     }
@@ -283,7 +295,7 @@ cudaError_t launch_head_fp4(const void* qh, const uint8_t* sfa, const void* qw, 
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kTcThreads);
+    cfg.blockDim = dim3(kFp4Threads);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -19,26 +19,31 @@ constexpr int kTcBN = 256;
 constexpr int kTcStages = 4;
 constexpr int kTc2Stages = 6;    // pair kernel: 32 KB stages (128 h rows + 128 W rows)
 constexpr int kTcThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-// NVFP4 head: vocabulary rows per tile, accumulator buffers and pipeline stages. TMEM holds
-// kFp4Acc accumulators of kFp4BN columns plus the scale factors of every stage in flight; of the
-// configurations that fit, 256-row tiles with one accumulator and 4 stages measured fastest (128-row
-// tiles with two accumulators re-read h twice as often and issue more scale copies per column).
+// NVFP4 head: vocabulary rows per tile, accumulator buffers, pipeline stages and threads. TMEM
+// holds kFp4Acc accumulators of kFp4BN columns plus the scale factors of every stage in flight; of
+// the configurations that fit, 256-row tiles with one accumulator measured fastest (128-row tiles
+// with two accumulators re-read h twice as often and issue more scale copies per column). Each
+// stage carries four copies of the w scale chunk (one per TMEM lane quadrant), which leaves shared
+// memory for 3 stages. 8 epilogue warps: two per lane quadrant, one per half of the tile's columns.
 constexpr int kFp4BN = 256;
 constexpr int kFp4Acc = 1;
-constexpr int kFp4Stages = 4;
+constexpr int kFp4Stages = 3;
+constexpr int kFp4Threads = 320;
 // Geometry of the fp32 CUDA-core head.
 constexpr int kSimtBM = 128;
 constexpr int kSimtBN = 64;
 
 // Work decomposition of a head pass: MB row blocks x NT vocabulary tiles, each row block split
 // into n_groups vocabulary groups (group g takes tiles g, g + n_groups, ...). A (row block,
-// group) unit writes one Partial per row into partials[row * n_groups + g].
+// group) unit writes `parts` Partials per row (one per column subset of its tiles) into
+// partials[row * n_groups * parts + g * parts + part].
 // For the CTA-pair kernel (pair = 1) a row block is 256 rows and `grid` counts pairs.
 struct HeadPlan {
     int R, V, d;
     int BM, BN;
     int MB, NT, n_groups, units, grid;
     int pair;
+    int parts;
 };
 
 HeadPlan plan_head(int R, int V, int d, int BM, int BN, int num_sms);
@@ -51,7 +56,7 @@ struct HeadArgs {
     float crow_base;          // inv_temp * log2(e)
     const float* h_scale;     // [R] or null
     const float* w_scale;     // [V] or null
-    float4* partials;         // [R][n_groups]: the partials of one row are contiguous
+    float4* partials;         // [R][n_groups * parts]: the partials of one row are contiguous
     uint32_t* status;         // sticky status word or null
     unsigned long long* timeline;  // loop timeline (dg_loop_params.trace_timeline) or null
     const int32_t* pass_ptr;       // loop mode: the pass index (device), else null

@@ -1,7 +1,7 @@
 // dg_nvfp4.cu -- NVFP4 operand preparation on the device:
 //   quant_rows_nvfp4_kernel  two-level NVFP4 quantisation of bf16 rows (the E4M3 rule's 4-bit
 //                            counterpart, applied to the hidden states in front of an NVFP4 head);
-//   pack_scales_kernel       plain [rows][d/16] block scales -> the 512-byte scale atoms the
+//   pack_scales_kernel       plain [rows][d/16] block scales -> the packed scale chunks the
 //                            block-scaled MMA's tensor-memory copies consume.
 // The NVFP4 rule, in IEEE binary32: amax = max_k |h_k|; amax == 0 gives row scale 1 and all
 // codes and block scales 0; otherwise g = fp32(amax / 2688) (2688 = 448 * 6) and, per block of
@@ -21,12 +21,19 @@ namespace {
 
 constexpr int kQThreads = 128;
 
-// Byte offset of (row, K block) inside the atom layout: atom (row / 128, block / 4) of 512 bytes,
-// byte (row % 32) * 16 + ((row % 128) / 32) * 4 + block % 4.
-__device__ __forceinline__ size_t sf_atom_offset(int row, int blk, int nks) {
-    const int g = row >> 7, m = row & 127;
-    return (static_cast<size_t>(g) * nks + (blk >> 2)) * 512 + (m & 31) * 16 + (m >> 5) * 4 +
-           (blk & 3);
+// Byte offset of (row, K block) in the packed layout: one 4096-byte chunk per (256-row group G,
+// 256-element K slice s) at (G * d/256 + s) * 4096; inside it, with m = row % 256, l = m % 32,
+// c = m / 32 and block = 16 s + 4 j + kb (j = 64-element MMA step of the slice):
+//   (l / 8) * 1024 + j * 256 + (c / 4) * 128 + (l % 8) * 16 + (c % 4) * 4 + kb.
+// Read as 8-row x 16-byte core matrices, a chunk holds for every step j the scale-factor tile of
+// the 256 rows (lane l, column c) with 8-row groups 1024 bytes apart: the source of one 128x256b
+// tensor-memory copy per step when four copies of the chunk sit 4096 bytes apart (one per lane
+// quadrant), and of a 32x128b copy of one 128-row half from byte j * 256 + half * 128.
+__device__ __forceinline__ size_t sf_offset(int row, int blk, int nslices) {
+    const int G = row >> 8, m = row & 255, l = m & 31, c = m >> 5;
+    const int s = blk >> 4, j = (blk >> 2) & 3, kb = blk & 3;
+    return (static_cast<size_t>(G) * nslices + s) * 4096 + (l >> 3) * 1024 + j * 256 +
+           (c >> 2) * 128 + (l & 7) * 16 + (c & 3) * 4 + kb;
 }
 
 __device__ __forceinline__ float e4m3_value(uint8_t c) {
@@ -52,9 +59,9 @@ __global__ void __launch_bounds__(kQThreads)
     grid_dependency_wait();
     grid_launch_dependents();
     const int r = blockIdx.x;
-    const int nb = d / 16, nks = d / 64;
+    const int nb = d / 16, nsl = d / 256;
     if (r >= R) {
-        for (int b = threadIdx.x; b < nb; b += kQThreads) sf[sf_atom_offset(r, b, nks)] = 0;
+        for (int b = threadIdx.x; b < nb; b += kQThreads) sf[sf_offset(r, b, nsl)] = 0;
         return;
     }
     const uint4* hr = reinterpret_cast<const uint4*>(h + static_cast<size_t>(r) * d);
@@ -76,7 +83,7 @@ __global__ void __launch_bounds__(kQThreads)
     if (amax == 0.f) {
         for (int b = threadIdx.x; b < nb; b += kQThreads) {
             qr[b] = make_uint2(0u, 0u);
-            sf[sf_atom_offset(r, b, nks)] = 0;
+            sf[sf_offset(r, b, nsl)] = 0;
         }
         if (threadIdx.x == 0) scale[r] = 1.0f;
         return;
@@ -97,7 +104,7 @@ __global__ void __launch_bounds__(kQThreads)
         for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(x[i]));
         const uint8_t sb = static_cast<uint8_t>(
             __nv_cvt_float_to_fp8(__fdiv_rn(bmax, g6), __NV_SATFINITE, __NV_E4M3));
-        sf[sf_atom_offset(r, b, nks)] = sb;
+        sf[sf_offset(r, b, nsl)] = sb;
         const float sv = e4m3_value(sb);
         uint32_t packed[2] = {0u, 0u};
         if (sv != 0.f) {
@@ -118,12 +125,12 @@ __global__ void __launch_bounds__(kQThreads)
 // One thread per (padded row, block): plain [rows][d/16] -> atoms; rows >= rows_in get 0.
 __global__ void pack_scales_kernel(const uint8_t* __restrict__ plain, int rows_in, int rows_pad,
                                    int d, uint8_t* __restrict__ packed) {
-    const int nb = d / 16, nks = d / 64;
+    const int nb = d / 16, nsl = d / 256;
     const size_t total = static_cast<size_t>(rows_pad) * nb;
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
         const int r = static_cast<int>(i / nb), b = static_cast<int>(i % nb);
-        packed[sf_atom_offset(r, b, nks)] = r < rows_in ? plain[i] : 0;
+        packed[sf_offset(r, b, nsl)] = r < rows_in ? plain[i] : 0;
     }
 }
 

@@ -312,13 +312,15 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, 
         : "memory");
 }
 
-// Shared-memory descriptor of a 32-row x 16-byte matrix stored row-major without swizzle
-// (four 8-row core matrices 128 bytes apart): the source of a 32x128b tensor-memory copy.
-__device__ __forceinline__ uint64_t sdesc_rows16_noswizzle(uint32_t saddr) {
+// Shared-memory descriptor of a matrix stored without swizzle as 8-row x 16-byte core matrices
+// (128 contiguous bytes each): `lbo` bytes between core matrices adjacent along the row (the
+// 16-byte chunks of a wider row), `sbo` bytes between successive 8-row groups. The source of a
+// tensor-memory copy.
+__device__ __forceinline__ uint64_t sdesc_noswizzle(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>(128 >> 4) << 16;   // leading byte offset (one core matrix along K)
-    d |= static_cast<uint64_t>(128 >> 4) << 32;   // stride byte offset: next 8 rows
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
     d |= static_cast<uint64_t>(1) << 46;          // descriptor version
     return d;                                      // swizzle mode 0 (none)
 }
@@ -327,6 +329,13 @@ __device__ __forceinline__ uint64_t sdesc_rows16_noswizzle(uint32_t saddr) {
 // four lane quadrants (each warp's 32 lanes see the same 4 columns).
 __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+
+// Copy 128 lanes x 256 bits (8 columns) from shared memory into tensor memory at `taddr`: lane L
+// receives source row L.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc)
                  : "memory");
 }
 
