@@ -43,4 +43,24 @@ __device__ __forceinline__ void drain_tile(RowState& st, uint32_t taddr0, const 
     }
 }
 
+// The same fold for NCOL columns already loaded into registers (v, multiple of 32 columns), so
+// that the accumulator can be handed back to the MMAs before the arithmetic runs.
+template <int KIND, int NCOL>
+__device__ __forceinline__ void fold_columns(RowState& st, float (&v)[NCOL], const float* csc,
+                                             float crow, int n_base, int valid_tile) {
+#pragma unroll
+    for (int c = 0; c < NCOL / 32; ++c) {
+        float(&w)[32] = *reinterpret_cast<float(*)[32]>(v + c * 32);
+        if (KIND == 1) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) w[j] *= csc[c * 32 + j];
+        }
+        const int valid = valid_tile - c * 32;
+        if (valid >= 32)
+            row_state_update<false>(st, w, crow, n_base + c * 32, 32);
+        else if (valid > 0)
+            row_state_update<true>(st, w, crow, n_base + c * 32, valid);
+    }
+}
+
 }  // namespace dg

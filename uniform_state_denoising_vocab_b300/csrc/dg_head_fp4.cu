@@ -29,8 +29,9 @@
 //              half of the tile's 256 columns into its own running state, so a unit writes two
 //              partials per row.
 // The scale factors of every stage in flight share the 512 TMEM columns with the accumulator, so
-// a 256-column tile has a single accumulator and its epilogue does not overlap the next tile's
-// MMAs. Scale copies are issued in order with the MMAs and cost about the same per instruction
+// a 256-column tile has a single accumulator; each epilogue thread loads its 128 columns into
+// registers in one TMEM load and releases the accumulator before folding them, so the softmax
+// arithmetic of a tile overlaps the MMAs of the next. Scale copies are issued in order with the MMAs and cost about the same per instruction
 // whatever their size, which is why the w scales travel as one 128x256b copy per step rather than
 // two replicated 32x128b copies.
 #include <cuda.h>
@@ -55,6 +56,7 @@ constexpr int EPI_WARPS = kFp4Threads / 32 - 2;  // two per lane quadrant
 constexpr int HALF = BN / 2;                     // columns per epilogue warp
 static_assert(BN == 256, "a w scale chunk covers 256 vocabulary rows");
 static_assert(EPI_WARPS == 8, "two epilogue warps per lane quadrant");
+static_assert(HALF == 128, "one 32x32b.x128 TMEM load per epilogue warp and tile");
 constexpr int TMEM_COLS = 512;
 constexpr uint32_t SF_COL0 = NACC * BN;          // scale-factor columns after the accumulators
 constexpr uint32_t SFB_COLS = BN / 32;           // scale columns of B per MMA
@@ -255,10 +257,14 @@ __global__ void __launch_bounds__(kFp4Threads, 1)
                 tc_fence_after();
                 const uint32_t taddr0 =
                     tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * BN + half * HALF;
-                drain_tile<1, HALF>(st, taddr0, csc, crow, n_base, args.V - n_base);
+                // take the 128 columns into registers and hand the accumulator back at once: the
+                // arithmetic below overlaps the next tile's MMAs
+                float v[HALF];
+                tmem_ld128(taddr0, v);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
+                fold_columns<1, HALF>(st, v, csc, crow, n_base, args.V - n_base);
             }
             if (ok && row < args.R)
                 args.partials[static_cast<size_t>(row) * parts_per_row + 2 * grp + half] =
