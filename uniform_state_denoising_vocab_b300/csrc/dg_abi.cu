@@ -71,7 +71,11 @@ enum Path {
     PATH_FP4_QUANT = 5       // bf16 h quantised to NVFP4 on the device
 };
 
-inline bool quant_path(int path) { return path == PATH_TC_E4M3_QUANT || path == PATH_FP4_QUANT; }
+// Paths with a preparation kernel in front of the head: quantisation of h, or (NVFP4 h) the
+// repack of its block scales into the head's row-block layout.
+inline bool quant_path(int path) {
+    return path == PATH_TC_E4M3_QUANT || path == PATH_FP4_QUANT || path == PATH_FP4;
+}
 
 struct DeviceInfo {
     int sms = 0;
@@ -184,7 +188,10 @@ int layout_for(const dg_head_desc* d, int path, const DeviceInfo& di, Layout* L)
         L->off_sch = off;
         off = up256(off + static_cast<size_t>(R) * 4);
         L->off_sfh = off;
-        off = up256(off + static_cast<size_t>(nvfp4_rows_pad(R)) * (d->d / 16));
+        off = up256(off + nvfp4_rowblock_bytes(R, d->d));
+    } else if (path == PATH_FP4) {
+        L->off_sfh = off;  // the caller's h block scales in the head's row-block layout
+        off = up256(off + nvfp4_rowblock_bytes(R, d->d));
     }
     L->total = off;
     return DG_OK;
@@ -226,7 +233,10 @@ cudaError_t launch_quantiser(const dg_head_desc* d, const Prepared& P, uint8_t* 
     if (P.path == PATH_FP4_QUANT)
         return launch_quant_rows_nvfp4(static_cast<const uint16_t*>(d->h), pl.R, pl.d,
                                        ws + P.L.off_qh, ws + P.L.off_sfh,
-                                       reinterpret_cast<float*>(ws + P.L.off_sch), status, stream);
+                                       reinterpret_cast<float*>(ws + P.L.off_sch), status, stream,
+                                       1);
+    if (P.path == PATH_FP4)
+        return launch_repack_rowblock(d->h_block_scale, pl.R, pl.d, ws + P.L.off_sfh, stream);
     return launch_quant_rows(static_cast<const uint16_t*>(d->h), pl.R, pl.d, ws + P.L.off_qh,
                              reinterpret_cast<float*>(ws + P.L.off_sch), status, stream);
 }
@@ -292,8 +302,13 @@ cudaError_t launch_head_only(const dg_head_desc* d, const Prepared& P, uint8_t* 
         a.num_kb = (pl.d + 127) / 128;
         return launch_head_tc(1, d->h, d->w, a, pl, stream);
     case PATH_FP4:
+    case -PATH_FP4:
+        if (P.path > 0) {
+            e = launch_quantiser(d, P, ws, status, stream);
+            if (e != cudaSuccess) return e;
+        }
         a.num_kb = pl.d / 256;
-        return launch_head_fp4(d->h, d->h_block_scale, d->w, d->w_block_scale, a, pl.grid, stream);
+        return launch_head_fp4(d->h, ws + P.L.off_sfh, d->w, d->w_block_scale, a, pl.grid, stream);
     case PATH_FP4_QUANT:
     case -PATH_FP4_QUANT: {
         if (P.path > 0) {

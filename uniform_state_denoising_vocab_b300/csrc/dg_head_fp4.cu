@@ -10,30 +10,30 @@
 //
 // Operand layouts (device, prepared by dg_quantize_nvfp4 / dg_nvfp4_pack_scales):
 //   codes: [rows][d/2] bytes, element 2j in the low nibble of byte j;
-//   block scales: one 4096-byte chunk per (256-row group, 256-element K slice), in the order the
-//     tensor-memory copies read (layout in dg_nvfp4.cu). The block-scaled MMA reads the scale of
-//     tile row m (lane quadrant q = m / 32) for a 64-element step from TMEM lane m, column
-//     (scale column + q); the scales of the 256 w rows of a step occupy 8 columns of every lane
-//     quadrant.
+//   block scales of w: packed, one 4096-byte chunk per (256-row group, 256-element K slice);
+//   block scales of h: the row-block layout, two 4096-byte tiles per (128-row block, K slice)
+//     (both layouts in dg_nvfp4.cu). The block-scaled MMA reads the scale of tile row m (lane
+//     quadrant q = m / 32) for a 64-element step from TMEM lane m, column (scale address + q);
+//     the scales of the 256 w rows of a step occupy 8 columns of every lane quadrant.
 //
 // Structure (one CTA of 320 threads per SM; 128 x 256 tiles; K slices of 256 elements):
-//   warp 0     TMA loads of the A / B code slices (128-byte swizzle) and bulk loads of the scale
-//              chunks into a 3-stage ring: the h chunk once, the w chunk four times (one copy
+//   warp 0     TMA loads of the A / B code slices (128-byte swizzle) and bulk loads of the scales
+//              into a 3-stage ring: the h row block's two tiles, the w chunk four times (one copy
 //              per lane quadrant, so that a single 128x256b copy fills all four);
 //   warp 1     owns 512 TMEM columns: the accumulator and one set of scale-factor columns per
-//              stage; one thread copies each stage's scales into tensor memory (per 64-element
-//              step: a 32x128b copy of the h row block's half, replicated over the lane quadrants,
-//              and a 128x256b copy of the w scales) and issues 4 block-scaled MMAs (M=128, N=256,
-//              K=64);
+//              stage; one thread copies each stage's scales into tensor memory (two 128x256b
+//              copies of h scales, one per pair of 64-element steps; one 128x256b copy of w
+//              scales per step) and issues 4 block-scaled MMAs (M=128, N=256, K=64);
 //   warps 2-9  epilogue: two warps per lane quadrant (one slot row per thread), each folding one
 //              half of the tile's 256 columns into its own running state, so a unit writes two
 //              partials per row.
 // The scale factors of every stage in flight share the 512 TMEM columns with the accumulator, so
 // a 256-column tile has a single accumulator; each epilogue thread loads its 128 columns into
 // registers in one TMEM load and releases the accumulator before folding them, so the softmax
-// arithmetic of a tile overlaps the MMAs of the next. Scale copies are issued in order with the MMAs and cost about the same per instruction
-// whatever their size, which is why the w scales travel as one 128x256b copy per step rather than
-// two replicated 32x128b copies.
+// arithmetic of a tile overlaps the MMAs of the next. Scale copies are issued in order with the
+// MMAs and cost time per instruction (the quadrant-replicating 32x128b.warpx4 form about twice a
+// 128x256b copy), so every scale tile is laid out for 128x256b copies: 6 per K slice instead of
+// 12 replicated ones.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -49,7 +49,7 @@ constexpr int BM = 128, BN = kFp4BN, NACC = kFp4Acc, STAGES = kFp4Stages;
 constexpr int A_BYTES = BM * 128;
 constexpr int B_BYTES = BN * 128;
 constexpr int SF_CHUNK = 4096;                   // packed scales of 256 rows x one K slice
-constexpr int SFA_BYTES = SF_CHUNK;              // the chunk holding this row block's scales
+constexpr int SFA_BYTES = 2 * 4096;             // row-block layout: two 128x256b copy sources
 constexpr int SFB_BYTES = 4 * SF_CHUNK;          // the w chunk once per TMEM lane quadrant
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
 constexpr int EPI_WARPS = kFp4Threads / 32 - 2;  // two per lane quadrant
@@ -148,10 +148,10 @@ __global__ void __launch_bounds__(kFp4Threads, 1)
                                     &ctl->full[stage], pol_h);
                         tma_load_2d(sB + stage * B_BYTES, &tmB, kb * 128, nb * BN,
                                     &ctl->full[stage], pol_w);
-                        // scale chunks of the slice: the h chunk once, the w chunk per quadrant
+                        // scales of the slice: the h row block's tiles, the w chunk per quadrant
                         bulk_load(sSFA + stage * SFA_BYTES,
-                                  sfa_g + (static_cast<size_t>(mb >> 1) * nsl + kb) * SF_CHUNK,
-                                  SF_CHUNK, &ctl->full[stage]);
+                                  sfa_g + (static_cast<size_t>(mb) * nsl + kb) * SFA_BYTES,
+                                  SFA_BYTES, &ctl->full[stage]);
                         const uint8_t* wchunk =
                             sfb_g + (static_cast<size_t>(nb) * nsl + kb) * SF_CHUNK;
                         for (int q = 0; q < 4; ++q)
@@ -181,7 +181,6 @@ __global__ void __launch_bounds__(kFp4Threads, 1)
             bool ok = true;
             for (int unit = blockIdx.x; unit < units && ok; unit += gridDim.x) {
                 const int grp = unit / args.MB;
-                const uint32_t a_half = ((unit % args.MB) & 1) * 128;  // row block's half of the chunk
                 for (int nb = grp; nb < args.NT && ok; nb += args.n_groups, ++tcount) {
                     const uint32_t buf = tcount % NACC, tph = (tcount / NACC) & 1u;
                     if (!mbar_wait(&ctl->tempty[buf], tph ^ 1u, abort_flag)) {
@@ -201,16 +200,17 @@ __global__ void __launch_bounds__(kFp4Threads, 1)
                         const uint32_t sf_col = tmem_base + SF_COL0 + stage * SF_COLS_PER_STAGE;
                         const uint32_t sa = smem_u32(sSFA + stage * SFA_BYTES);
                         const uint32_t sb = smem_u32(sSFB + stage * SFB_BYTES);
-                        // step j: h scales from byte j * 256 + a_half of the chunk (8-row
-                        // groups 1024 bytes apart), replicated over the lane quadrants; w scales
-                        // from byte j * 256 of the four chunk copies (quadrant q's rows 4096 q on)
+                        // h scales: steps 2p, 2p + 1 from tile p of the row-block layout into
+                        // columns 8p .. 8p + 7 (step j's scale address: column 4j); w scales of
+                        // step j from byte j * 256 of the four chunk copies (quadrant q's rows
+                        // 4096 q on; 8-row groups 1024 bytes apart) into 8 columns
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            tmem_cp_32x128b_x4(sf_col + 4 * j,
-                                               sdesc_noswizzle(sa + j * 256 + a_half, 1024, 1024));
+                        for (int p = 0; p < 2; ++p)
+                            tmem_cp_128x256b(sf_col + 8 * p, sdesc_noswizzle(sa + p * 4096, 128, 256));
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
                             tmem_cp_128x256b(sf_col + 16 + SFB_COLS * j,
                                              sdesc_noswizzle(sb + j * 256, 128, 1024));
-                        }
                         const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sA + stage * A_BYTES));
                         const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sB + stage * B_BYTES));
 #pragma unroll

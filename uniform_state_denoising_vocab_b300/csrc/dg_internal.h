@@ -117,13 +117,20 @@ cudaError_t launch_head_tc2(int kind, const CUtensorMap& ma, const CUtensorMap& 
                             const HeadArgs& args, int n_pairs, cudaStream_t stream);
 // Resident clusters of the pair kernel on the current device (0 if it cannot run).
 int head_tc2_max_pairs();
-// NVFP4 head (single-CTA, block-scaled MMAs): codes + packed block scales of h and w.
+// NVFP4 head (single-CTA, block-scaled MMAs): codes of h and w, h block scales in the row-block
+// layout, w block scales packed.
 cudaError_t launch_head_fp4(const void* qh, const uint8_t* sfa, const void* qw, const uint8_t* sfb,
                             const HeadArgs& args, int grid, cudaStream_t stream);
-// NVFP4 preparation (dg_nvfp4.cu). Packed block-scale arrays cover nvfp4_rows_pad(rows) rows.
+// NVFP4 preparation (dg_nvfp4.cu). Packed block-scale arrays cover nvfp4_rows_pad(rows) rows;
+// the row-block layout of the head's A operand takes nvfp4_rowblock_bytes(rows, d) bytes.
+// layout: 0 = packed (dg_nvfp4_pack_scales), 1 = row-block.
 int nvfp4_rows_pad(int rows);
+size_t nvfp4_rowblock_bytes(int rows, int d);
 cudaError_t launch_quant_rows_nvfp4(const uint16_t* h, int R, int d, uint8_t* q, uint8_t* sf,
-                                    float* scale, uint32_t* status, cudaStream_t stream);
+                                    float* scale, uint32_t* status, cudaStream_t stream,
+                                    int layout = 0);
+cudaError_t launch_repack_rowblock(const uint8_t* packed, int R, int d, uint8_t* out,
+                                   cudaStream_t stream);
 cudaError_t launch_pack_scales(const uint8_t* plain, int rows, int d, uint8_t* packed,
                                cudaStream_t stream);
 // fp32 CUDA-core head.

@@ -2,7 +2,10 @@
 //   quant_rows_nvfp4_kernel  two-level NVFP4 quantisation of bf16 rows (the E4M3 rule's 4-bit
 //                            counterpart, applied to the hidden states in front of an NVFP4 head);
 //   pack_scales_kernel       plain [rows][d/16] block scales -> the packed scale chunks the
-//                            block-scaled MMA's tensor-memory copies consume.
+//                            block-scaled MMA's tensor-memory copies consume;
+//   repack_rowblock_kernel   packed scales of the slot rows -> the row-block layout the head
+//                            reads for its A operand (the quantiser writes it directly when h
+//                            is quantised inside a pass).
 // The NVFP4 rule, in IEEE binary32: amax = max_k |h_k|; amax == 0 gives row scale 1 and all
 // codes and block scales 0; otherwise g = fp32(amax / 2688) (2688 = 448 * 6) and, per block of
 // 16 elements with bmax = max |h_k|, sb = e4m3_rn_satfinite(fp32(bmax / fp32(6 g))); a zero sb
@@ -36,6 +39,25 @@ __device__ __forceinline__ size_t sf_offset(int row, int blk, int nslices) {
            (c >> 2) * 128 + (l & 7) * 16 + (c & 3) * 4 + kb;
 }
 
+// Byte offset of (row, K block) in the row-block layout of the head's A operand: per (128-row
+// block b, 256-element K slice s, pair p of 64-element steps) a 4096-byte tile of 128 rows x 32
+// bytes (8-row x 16-byte core matrices, 8-row groups 256 bytes apart, the second 16 bytes of a
+// row 128 bytes on), read by one 128x256b tensor-memory copy into 8 columns. Row L = 32 q + l of
+// the block holds the scales of step 2 p + jj at bytes jj * 16 + q * 4 .. + 3 of its 32: column
+// 4 jj + q, the column the block-scaled MMA reads for lane quadrant q when the step's scale
+// address is column 4 jj. The other bytes are never read.
+//   ((b * d/256 + s) * 2 + p) * 4096 + (L / 8) * 256 + jj * 128 + (L % 8) * 16 + q * 4 + kb
+__device__ __forceinline__ size_t sf_rowblock_offset(int row, int blk, int nslices) {
+    const int b = row >> 7, L = row & 127;
+    const int s = blk >> 4, j = (blk >> 2) & 3, kb = blk & 3;
+    return ((static_cast<size_t>(b) * nslices + s) * 2 + (j >> 1)) * 4096 + (L >> 3) * 256 +
+           (j & 1) * 128 + (L & 7) * 16 + (L >> 5) * 4 + kb;
+}
+
+__device__ __forceinline__ size_t sf_out_offset(int layout, int row, int blk, int nslices) {
+    return layout == 0 ? sf_offset(row, blk, nslices) : sf_rowblock_offset(row, blk, nslices);
+}
+
 __device__ __forceinline__ float e4m3_value(uint8_t c) {
     __nv_fp8_e4m3 v;
     v.__x = c;
@@ -49,19 +71,19 @@ __device__ __forceinline__ float block_max_q(float v, float* red) {
     return fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
 }
 
-// Grid: rows_pad CTAs of kQThreads (rows_pad = R rounded up to 256); rows >= R only zero their
-// block scales.
+// Grid: one CTA of kQThreads per row of the scale layout (R rounded up to 256 for the packed
+// layout, to 128 for the row-block layout); rows >= R only zero their block scales.
 __global__ void __launch_bounds__(kQThreads)
     quant_rows_nvfp4_kernel(const __nv_bfloat16* __restrict__ h, int R, int d,
                             uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
-                            float* __restrict__ scale, uint32_t* status) {
+                            float* __restrict__ scale, uint32_t* status, int layout) {
     __shared__ float red[4];
     grid_dependency_wait();
     grid_launch_dependents();
     const int r = blockIdx.x;
     const int nb = d / 16, nsl = d / 256;
     if (r >= R) {
-        for (int b = threadIdx.x; b < nb; b += kQThreads) sf[sf_offset(r, b, nsl)] = 0;
+        for (int b = threadIdx.x; b < nb; b += kQThreads) sf[sf_out_offset(layout, r, b, nsl)] = 0;
         return;
     }
     const uint4* hr = reinterpret_cast<const uint4*>(h + static_cast<size_t>(r) * d);
@@ -83,7 +105,7 @@ __global__ void __launch_bounds__(kQThreads)
     if (amax == 0.f) {
         for (int b = threadIdx.x; b < nb; b += kQThreads) {
             qr[b] = make_uint2(0u, 0u);
-            sf[sf_offset(r, b, nsl)] = 0;
+            sf[sf_out_offset(layout, r, b, nsl)] = 0;
         }
         if (threadIdx.x == 0) scale[r] = 1.0f;
         return;
@@ -104,7 +126,7 @@ __global__ void __launch_bounds__(kQThreads)
         for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(x[i]));
         const uint8_t sb = static_cast<uint8_t>(
             __nv_cvt_float_to_fp8(__fdiv_rn(bmax, g6), __NV_SATFINITE, __NV_E4M3));
-        sf[sf_offset(r, b, nsl)] = sb;
+        sf[sf_out_offset(layout, r, b, nsl)] = sb;
         const float sv = e4m3_value(sb);
         uint32_t packed[2] = {0u, 0u};
         if (sv != 0.f) {
@@ -134,14 +156,33 @@ __global__ void pack_scales_kernel(const uint8_t* __restrict__ plain, int rows_i
     }
 }
 
+// One thread per (row of the row-block layout, block): packed -> row-block; rows >= R get 0.
+__global__ void repack_rowblock_kernel(const uint8_t* __restrict__ packed, int R, int rows_out,
+                                       int d, uint8_t* __restrict__ out) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int nb = d / 16, nsl = d / 256;
+    const size_t total = static_cast<size_t>(rows_out) * nb;
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const int r = static_cast<int>(i / nb), b = static_cast<int>(i % nb);
+        out[sf_rowblock_offset(r, b, nsl)] = r < R ? packed[sf_offset(r, b, nsl)] : 0;
+    }
+}
+
 }  // namespace
 
 int nvfp4_rows_pad(int rows) { return (rows + 255) / 256 * 256; }
 
+size_t nvfp4_rowblock_bytes(int rows, int d) {
+    return static_cast<size_t>((rows + 127) / 128) * 128 * (d / 16) * 4;
+}
+
 cudaError_t launch_quant_rows_nvfp4(const uint16_t* h, int R, int d, uint8_t* q, uint8_t* sf,
-                                    float* scale, uint32_t* status, cudaStream_t stream) {
+                                    float* scale, uint32_t* status, cudaStream_t stream,
+                                    int layout) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(nvfp4_rows_pad(R));
+    cfg.gridDim = dim3(layout == 0 ? nvfp4_rows_pad(R) : (R + 127) / 128 * 128);
     cfg.blockDim = dim3(kQThreads);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -149,7 +190,24 @@ cudaError_t launch_quant_rows_nvfp4(const uint16_t* h, int R, int d, uint8_t* q,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, quant_rows_nvfp4_kernel,
-                              reinterpret_cast<const __nv_bfloat16*>(h), R, d, q, sf, scale, status);
+                              reinterpret_cast<const __nv_bfloat16*>(h), R, d, q, sf, scale, status,
+                              layout);
+}
+
+cudaError_t launch_repack_rowblock(const uint8_t* packed, int R, int d, uint8_t* out,
+                                   cudaStream_t stream) {
+    const int rows_out = (R + 127) / 128 * 128;
+    const size_t total = static_cast<size_t>(rows_out) * (d / 16);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((total + 255) / 256 < 148 * 8 ? (total + 255) / 256
+                                                                            : 148 * 8));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    set_pdl_attr(&attr[0]);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, repack_rowblock_kernel, packed, R, rows_out, d, out);
 }
 
 cudaError_t launch_pack_scales(const uint8_t* plain, int rows, int d, uint8_t* packed,
