@@ -154,17 +154,21 @@ DATASHEET = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0, "e4m3_tflops": 4500.0}
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the head kernel,
 # from an ncu capture of the build whose head sources hash to `src` (summaries in profiles/).
 # A different hash means the kernel changed since the counters were taken: traffic is null.
-HEAD_SOURCES = ["dg_head_tc2.cu", "dg_head_epi.cuh", "dg_common.cuh", "dg_ptx.cuh", "dg_internal.h"]
+HEAD_SOURCES = {
+    "tc2": ["dg_head_tc2.cu", "dg_head_epi.cuh", "dg_common.cuh", "dg_ptx.cuh", "dg_internal.h"],
+    "fp4": ["dg_head_fp4.cu", "dg_head_epi.cuh", "dg_common.cuh", "dg_ptx.cuh", "dg_internal.h"],
+}
 TRAFFIC = {
-    "pass_bf16_v262144_d2816": {"bytes": 1.477923e9 + 3.30496e6, "src": "089d8a0aad9fefb0"},
-    "loop_e4m3_v262144_d2816": {"bytes": 740.054784e6 + 2.882816e6, "src": "089d8a0aad9fefb0"},
+    "pass_bf16_v262144_d2816": {"bytes": 1.477922e9 + 3.227648e6, "src": "5806b221557a181a"},
+    "loop_e4m3_v262144_d2816": {"bytes": 740.031488e6 + 2.866432e6, "src": "5806b221557a181a"},
+    "pass_nvfp4_v262144_d2816": {"bytes": 417.411584e6 + 3.492864e6, "src": "8b34dc2a8d024d3f"},
 }
 
 
-def head_source_hash() -> str:
+def head_source_hash(kind: str = "tc2") -> str:
     import hashlib
     hsh = hashlib.sha256()
-    for f in HEAD_SOURCES:
+    for f in HEAD_SOURCES[kind]:
         with open(os.path.join(ROOT, "uniform_state_denoising_vocab_b300", "csrc", f), "rb") as fh:
             hsh.update(fh.read())
     return hsh.hexdigest()[:16]
@@ -194,7 +198,8 @@ def roofline(cfg, r, peaks, peak_kind, step_s):
                    peak_source=f"{peak_kind} sustained bf16 cuBLAS" +
                    (f" x{ratio:g} nominal {cfg.precision}/bf16" if ratio != 1.0 else ""))
     rec = TRAFFIC.get(cfg.name)
-    out["traffic"] = rec["bytes"] if rec and rec["src"] == head_source_hash() else None
+    kind = "fp4" if cfg.precision == "nvfp4" else "tc2"
+    out["traffic"] = rec["bytes"] if rec and rec["src"] == head_source_hash(kind) else None
     out["kernel"] = ("head_fp4_kernel" if cfg.precision == "nvfp4" else
                      {"f32": "head_simt_kernel", "bf16": "head_tc2_kernel<0>",
                       "e4m3": "head_tc2_kernel<1>"}[cfg.precision] if cfg.R > 128 or cfg.precision == "f32"
