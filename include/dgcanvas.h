@@ -319,6 +319,31 @@ DG_API int dg_canvas_step_noalloc(const dg_head_desc* desc, const int32_t* canva
                                   const dg_stop_rule* rule, uint32_t* status, dg_stream_t stream);
 
 /*
+ * One canvas pass on HOST buffers: the hidden states (desc->h, and desc->h_scale /
+ * desc->h_block_scale when h is E4M3 / NVFP4) and canvas_in [B*S] are read from host memory, the
+ * new canvas is written to canvas_out [B*S] and, if non-NULL, the per-canvas mean entropy to
+ * mean_entropy [B], both host memory. w, w_scale, w_block_scale, state and status stay device
+ * pointers; keep_k, seed, pass and rule are those of dg_canvas_step, whose pass this runs. (The
+ * pages describe no such entry point; it serves callers whose data lives on the host.)
+ * Everything is enqueued and the call returns: the uploads run on a copy stream owned by the
+ * library and are ordered before the pass on `stream` by events; the read-backs run on `stream`
+ * after the pass. Host results are valid once `stream` has synchronised; host inputs must stay
+ * valid and unchanged until then. Use page-locked host memory for the copies to be asynchronous.
+ * The device copies live in the workspace, in two staging sets used by successive calls in turn,
+ * so the uploads of one call overlap the previous call's kernels; a set is not rewritten before
+ * the pass that last used it has finished. Calls sharing a workspace must share `stream`. Not for
+ * use under stream capture (DG_ERR_UNSUPPORTED): capture dg_canvas_step instead.
+ * dg_workspace_bytes_host: workspace bytes for this entry point (dg_workspace_bytes plus the two
+ * staging sets).
+ */
+DG_API int dg_workspace_bytes_host(const dg_head_desc* desc, size_t* bytes);
+DG_API int dg_canvas_step_host(const dg_head_desc* desc, const int32_t* canvas_in,
+                               int32_t* canvas_out, float* mean_entropy, int32_t keep_k,
+                               uint64_t seed, uint32_t pass, dg_canvas_state* state,
+                               const dg_stop_rule* rule, void* workspace, size_t workspace_bytes,
+                               uint32_t* status, dg_stream_t stream);
+
+/*
  * Instrumentation: make the next dg_canvas_stats / dg_canvas_step call issued by this host
  * thread record `start_event` on its stream just before its vocabulary-head kernel and
  * `stop_event` just after it (cudaEvent_t handles created by the caller). One-shot; calls that

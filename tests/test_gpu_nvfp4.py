@@ -108,10 +108,13 @@ def test_nvfp4_pass_parity(dg, orc, B, S, V, d):
     assert np.allclose(g["mean_entropy"], o["mean_entropy"], atol=TOL["bf16"])
 
 
-def test_nvfp4_prequantised_h_matches_device_quantiser(dg):
-    """NVFP4 h quantised by dg_quantize_nvfp4 and passed in directly gives bit-identical
-    statistics to bf16 h quantised inside the pass."""
-    B, S, V, d = 1, 256, 1500, 512
+@pytest.mark.parametrize("B,S", [(1, 256), (2, 100), (1, 64)])
+def test_nvfp4_prequantised_h_matches_device_quantiser(dg, B, S):
+    """NVFP4 h quantised by dg_quantize_nvfp4 and passed in directly (its packed block scales
+    repacked into the head's row-block layout inside the pass) gives bit-identical statistics to
+    bf16 h quantised inside the pass (straight into the row-block layout), including row counts
+    that end inside a 128-row block."""
+    V, d = 1500, 512
     hb, _, tw, twb, tws, canvas = _nvfp4_case(dg, B, S, V, d, 77)
     th = dev_bf16(hb, (B * S, d))
     a = dg.dg_canvas_stats(th, tw, B=B, S=S, w_scale=tws, w_dtype=dg.DG_NVFP4, w_block_scale=twb)

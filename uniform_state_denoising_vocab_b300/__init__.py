@@ -107,6 +107,11 @@ def lib():
                                         C.POINTER(LoopParams), C.c_int32, C.c_float, C.c_float,
                                         vp, vp, vp, sz, vp, vp]
         L.dg_block_generate.restype = C.c_int
+        L.dg_workspace_bytes_host.argtypes = [C.POINTER(HeadDesc), C.POINTER(sz)]
+        L.dg_workspace_bytes_host.restype = C.c_int
+        L.dg_canvas_step_host.argtypes = [C.POINTER(HeadDesc), vp, vp, vp, C.c_int32, C.c_uint64,
+                                          C.c_uint32, vp, C.POINTER(StopRule), vp, sz, vp, vp]
+        L.dg_canvas_step_host.restype = C.c_int
         L.dg_profile_next_head.argtypes = [C.c_void_p, C.c_void_p]
         L.dg_profile_next_head.restype = C.c_int
         for f in ("dg_workspace_bytes", "dg_canvas_stats", "dg_canvas_step", "dg_canvas_loop"):
@@ -249,6 +254,67 @@ def dg_canvas_stats(h, w, *, B: int, S: int, h_scale=None, w_scale=None, inv_tem
     _check(rc, "dg_canvas_stats")
     out["status"] = st
     return out
+
+
+def _host_ptr(t):
+    if t is None:
+        return None
+    if t.device.type != "cpu":
+        raise ValueError("host buffers of dg_canvas_step_host must be CPU tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libdgcanvas must be contiguous")
+    return C.c_void_p(t.data_ptr())
+
+
+def host_desc(h, w, *, B: int, S: int, h_scale=None, h_block_scale=None, w_scale=None,
+              inv_temp: float = 1.0, **desc_kw) -> HeadDesc:
+    """Head descriptor whose h (and h_scale / h_block_scale) are host tensors, w on the device."""
+    hd = dtype_code(h) if "h_dtype" not in desc_kw else desc_kw.pop("h_dtype")
+    d_ = desc_kw.pop("d", None)
+    if d_ is None:
+        d_ = int(h.shape[1]) * (2 if hd == DG_NVFP4 else 1)
+    desc = make_desc(None, w, B=B, S=S, w_scale=w_scale, inv_temp=inv_temp, h_dtype=hd, d=d_,
+                     **desc_kw)
+    desc.h = _host_ptr(h).value
+    desc.h_scale = None if h_scale is None else _host_ptr(h_scale).value
+    desc.h_block_scale = None if h_block_scale is None else _host_ptr(h_block_scale).value
+    return desc
+
+
+def dg_workspace_bytes_host(desc: HeadDesc) -> int:
+    n = C.c_size_t(0)
+    _check(lib().dg_workspace_bytes_host(C.byref(desc), C.byref(n)), "dg_workspace_bytes_host")
+    return int(n.value)
+
+
+def dg_canvas_step_host(h, w, canvas_in, keep_k: int, seed: int, pass_: int, *, B: int, S: int,
+                        canvas_out=None, mean_entropy=None, h_scale=None, h_block_scale=None,
+                        w_scale=None, inv_temp: float = 1.0, state=None,
+                        rule: StopRule | None = None, workspace=None, status=None, stream=None,
+                        desc: HeadDesc | None = None, **desc_kw) -> dict:
+    """One canvas pass on host buffers: h [B*S, d] (and its scales) and canvas_in [B*S] are CPU
+    tensors (page-locked for asynchronous copies); the new canvas and the per-canvas mean entropy
+    are written to CPU tensors, valid once `stream` has synchronised. w stays on the device.
+    Pass a prebuilt `desc` (host_desc) and `workspace` to avoid per-call set-up."""
+    dev = w.device
+    if desc is None:
+        desc = host_desc(h, w, B=B, S=S, h_scale=h_scale, h_block_scale=h_block_scale,
+                         w_scale=w_scale, inv_temp=inv_temp, **desc_kw)
+    if workspace is None:
+        workspace = torch.empty(dg_workspace_bytes_host(desc), dtype=torch.uint8, device=dev)
+    R = B * S
+    if canvas_out is None:
+        canvas_out = torch.empty(R, dtype=torch.int32).pin_memory()
+    if mean_entropy is None:
+        mean_entropy = torch.empty(B, dtype=torch.float32).pin_memory()
+    st = torch.zeros(1, dtype=torch.int32, device=dev) if status is None else status
+    rc = lib().dg_canvas_step_host(C.byref(desc), _host_ptr(canvas_in), _host_ptr(canvas_out),
+                                   _host_ptr(mean_entropy), int(keep_k), C.c_uint64(seed),
+                                   C.c_uint32(pass_ & 0xFFFFFFFF), _ptr(state),
+                                   None if rule is None else C.byref(rule), _ptr(workspace),
+                                   workspace.numel(), _ptr(st), _stream(stream))
+    _check(rc, "dg_canvas_step_host")
+    return {"canvas": canvas_out, "mean_entropy": mean_entropy, "status": st}
 
 
 def pass_rule(keep_rule: int = KEEP_CONFIDENCE, mask_id: int | None = None,
