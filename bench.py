@@ -466,7 +466,6 @@ def oracle_sample(cfg, target_s: float = 15.0):
     head = make_head(cfg)
     w = head["w"]
     wsc = head["w_scale"]
-    rows = 1
     h = normal_f32(R * d, cfg.seed, TAG_H)
     if cfg.precision != "f32":
         h = f32_to_bf16_bits(h)
@@ -476,11 +475,15 @@ def oracle_sample(cfg, target_s: float = 15.0):
     if cfg.precision == "nvfp4":
         h, hb, hs = oracle.quant_rows_nvfp4(h, R, d)
     bkw = {} if cfg.precision != "nvfp4" else dict(h_bscale=hb, w_bscale=head["w_bscale"])
-    # calibrate with one row, then size the sample to roughly target_s seconds
-    t0 = time.perf_counter()
-    oracle.head_stats(R, d, V, cfg.precision, h, w, h_scale=hs, w_scale=wsc, rows=np.arange(rows),
+    # calibrate on one row per host thread (the oracle spreads rows over threads) after one
+    # warm-up row (thread start-up, first touch of W), then size the sample to roughly target_s
+    oracle.head_stats(R, d, V, cfg.precision, h, w, h_scale=hs, w_scale=wsc, rows=np.arange(1),
                       **bkw)
-    t1 = time.perf_counter() - t0
+    cal = min(max(1, oracle.num_threads()), R)
+    t0 = time.perf_counter()
+    oracle.head_stats(R, d, V, cfg.precision, h, w, h_scale=hs, w_scale=wsc,
+                      rows=np.arange(cal), **bkw)
+    t1 = (time.perf_counter() - t0) / cal
     rows = int(max(1, min(R, target_s / max(t1, 1e-6))))
     t0 = time.perf_counter()
     st = oracle.head_stats(R, d, V, cfg.precision, h, w, h_scale=hs, w_scale=wsc,
