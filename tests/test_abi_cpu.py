@@ -113,6 +113,26 @@ def test_step_argument_checks(dg):
                             None, None, 0, None, None) == -1
 
 
+def test_host_step_argument_checks(dg):
+    """dg_canvas_step_host rejects missing buffers and bad descriptors before any device work."""
+    desc = _desc(dg)
+    L = dg.lib()
+    n = C.c_size_t(0)
+    assert L.dg_workspace_bytes_host(None, C.byref(n)) == -1
+    assert L.dg_workspace_bytes_host(C.byref(desc), None) == -1
+    assert L.dg_workspace_bytes_host(C.byref(_desc(dg, B=0)), C.byref(n)) == -1
+    assert L.dg_workspace_bytes_host(C.byref(_desc(dg, w=8200)), C.byref(n)) == -2
+    # null canvases, null h or null workspace
+    assert L.dg_canvas_step_host(C.byref(desc), None, 16, None, 1, 0, 0, None, None, 256, 1 << 20,
+                                 None, None) == -1
+    assert L.dg_canvas_step_host(C.byref(desc), 16, None, None, 1, 0, 0, None, None, 256, 1 << 20,
+                                 None, None) == -1
+    assert L.dg_canvas_step_host(C.byref(_desc(dg, h=None)), 16, 16, None, 1, 0, 0, None, None,
+                                 256, 1 << 20, None, None) == -1
+    assert L.dg_canvas_step_host(C.byref(desc), 16, 16, None, 1, 0, 0, None, None, None, 1 << 20,
+                                 None, None) == -1
+
+
 def test_status_strings(dg):
     for code in (0, -1, -2, -3, -4, -5, 1, 2, 4):
         s = dg.dg_status_string(code)
