@@ -26,13 +26,52 @@
 namespace dg {
 namespace {
 
-__device__ __forceinline__ Partial shfl_xor_partial(const Partial& p, int off) {
-    Partial q;
-    q.mx = __shfl_xor_sync(0xffffffffu, p.mx, off);
-    q.s = __shfl_xor_sync(0xffffffffu, p.s, off);
-    q.u = __shfl_xor_sync(0xffffffffu, p.u, off);
-    q.idx = __shfl_xor_sync(0xffffffffu, p.idx, off);
-    return q;
+// The same monoid over several partials at once, maximum first: M = max mx, then every non-empty
+// term rescaled to M with its own 2^(mx - M) (independent special-function operations instead of
+// a chain of pairwise merges), S = sum 2^(mx - M) s, U = sum 2^(mx - M) (u + s (mx - M)), argmax
+// the lowest index among the terms attaining M. Empty partials (s = 0) contribute nothing; a
+// non-finite s or u propagates into the result, where the merge's finiteness check sees it.
+__device__ __forceinline__ Partial fold_max_first(const Partial (&p)[4]) {
+    float M = p[0].mx;
+#pragma unroll
+    for (int i = 1; i < 4; ++i) M = fmaxf(M, p[i].mx);
+    Partial r;
+    r.mx = M;
+    r.s = 0.f;
+    r.u = 0.f;
+    r.idx = 0x7FFFFFFF;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (p[i].s == 0.f) continue;
+        const float d = p[i].mx - M;
+        const float e = ex2_fast(d);
+        r.s = fmaf(e, p[i].s, r.s);
+        r.u = fmaf(e, fmaf(p[i].s, d, p[i].u), r.u);
+        if (p[i].mx == M) r.idx = min(r.idx, p[i].idx);
+    }
+    return r;
+}
+
+// Across the 32 lanes of a warp (each holding one partial): maximum by xor butterfly, each lane
+// rescales its own terms, then sums and the lowest attaining index by xor butterflies; every
+// lane ends with the same result (each butterfly step adds the same two values on both lanes).
+__device__ __forceinline__ Partial warp_fold_max_first(const Partial& a) {
+    float M = a.mx;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const bool live = a.s != 0.f;
+    const float d = a.mx - M;
+    const float e = live ? ex2_fast(d) : 0.f;
+    float S = live ? e * a.s : 0.f;
+    float U = live ? e * fmaf(a.s, d, a.u) : 0.f;
+    int idx = (live && a.mx == M) ? a.idx : 0x7FFFFFFF;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        S += __shfl_xor_sync(0xffffffffu, S, off);
+        U += __shfl_xor_sync(0xffffffffu, U, off);
+        idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, off));
+    }
+    return Partial{M, S, U, idx};
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -66,9 +105,9 @@ struct MergeSmem {
 
 // Cluster b (kMergeCluster CTAs of kMergeThreads) handles canvas b. CTA c owns slots
 // [c * rpc, (c + 1) * rpc) with rpc = ceil(S / kMergeCluster); warp w merges the vocabulary-group
-// partials of its slots w, w + 16, ...: lane l takes groups l, l + 32, ... in increasing order,
-// then the lanes combine with a fixed xor butterfly (lower lane first), so every run merges in
-// the same order and all lanes end with the same result. After a cluster barrier every CTA reads
+// partials of its slots w, w + 32, ...: lane l takes groups l, l + 32, ..., four at a time
+// (maximum first), then the lanes combine maximum first with fixed xor butterflies, so every run
+// merges in the same order and all lanes end with the same result. After a cluster barrier every CTA reads
 // the whole canvas's confidences from the cluster's shared memory and ranks its own slots by
 // (key desc, slot asc), the key being the confidence or the negated entropy: kept <=> rank < K;
 // kept slots take their argmax, the others the counter-hash draw (or the mask token). CTA 0 forms the mean entropy (fixed-order pairwise tree over the slots) and,
@@ -131,14 +170,12 @@ __global__ void __cluster_dims__(kMergeCluster, 1, 1) __maxnreg__(40)
                                         draw_key(a.seed, static_cast<uint32_t>(p),
                                                  row_off + static_cast<uint64_t>(r)),
                                         static_cast<uint32_t>(a.V), a.inv_v));
+            Partial pc[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc = partial_merge(acc, unpack(v[i]));
+            for (int i = 0; i < 4; ++i) pc[i] = unpack(v[i]);
+            acc = partial_merge(acc, fold_max_first(pc));
         }
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const Partial o = shfl_xor_partial(acc, off);
-            acc = (lane & off) ? partial_merge(o, acc) : partial_merge(acc, o);
-        }
+        acc = warp_fold_max_first(acc);
         if (lane == 0 && !frozen) {
             const float s = acc.s;
             sm.conf[jj] = 1.0f / s;
