@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kQThreads)
     if (threadIdx.x == 0) scale[r] = g;
 }
 
-// One thread per (padded row, block): plain [rows][d/16] -> atoms; rows >= rows_in get 0.
+// One thread per (padded row, block): plain [rows][d/16] -> packed chunks; rows >= rows_in get 0.
 __global__ void pack_scales_kernel(const uint8_t* __restrict__ plain, int rows_in, int rows_pad,
                                    int d, uint8_t* __restrict__ packed) {
     const int nb = d / 16, nsl = d / 256;
