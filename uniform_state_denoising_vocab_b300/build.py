@@ -17,7 +17,7 @@ OUT = PKG / "libdgcanvas.so"
 OBJ = PKG / "_build"
 SOURCES = ["dg_abi.cu", "dg_head_tc.cu", "dg_head_tc2.cu", "dg_head_fp4.cu", "dg_nvfp4.cu", "dg_head_simt.cu",
            "dg_sampler.cu", "dg_noalloc.cu", "dg_host.cu"]
-HEADERS = ["dg_common.cuh", "dg_head_epi.cuh", "dg_ptx.cuh", "dg_internal.h"]
+HEADERS = ["dg_common.cuh", "dg_head_epi.cuh", "dg_ptx.cuh", "dg_internal.h", "dg_nvtx.h"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
          "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden", "-I", str(INCLUDE),

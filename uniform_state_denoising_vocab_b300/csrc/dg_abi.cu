@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "../../include/dgcanvas.h"
+#include "dg_nvtx.h"
 #include "dg_internal.h"
 
 namespace dg {
@@ -423,6 +424,7 @@ int dg_workspace_bytes(const dg_head_desc* desc, size_t* bytes) {
 int dg_canvas_stats(const dg_head_desc* desc, int32_t* argmax, float* conf, float* entropy,
                     float* mean_entropy, void* workspace, size_t workspace_bytes, uint32_t* status,
                     dg_stream_t stream) {
+    dg::NvtxRange nvtx_range("dg_canvas_stats");
     Prepared P;
     int rc = prepare(desc, workspace, workspace_bytes, &P);
     if (rc != DG_OK) return rc;
@@ -441,6 +443,7 @@ int dg_canvas_step(const dg_head_desc* desc, const int32_t* canvas_in, int32_t* 
                    float* entropy, uint8_t* kept, float* mean_entropy, dg_canvas_state* state,
                    const dg_stop_rule* rule, void* workspace, size_t workspace_bytes,
                    uint32_t* status, dg_stream_t stream) {
+    dg::NvtxRange nvtx_range("dg_canvas_step");
     if (!canvas_in || !canvas_out || keep_k < 0) return DG_ERR_INVALID_ARG;
     if (state && !rule) return DG_ERR_INVALID_ARG;
     if (rule && (rule->max_passes < 1 || rule->stable_passes < 1 ||
@@ -720,6 +723,7 @@ extern "C" int dg_canvas_loop(const dg_head_desc* desc, int32_t* canvas, void* h
                               dg_canvas_state* state, int32_t* argmax, float* conf, float* entropy,
                               void* workspace, size_t workspace_bytes, uint32_t* status,
                               dg_stream_t stream) {
+    dg::NvtxRange nvtx_range("dg_canvas_loop");
     using namespace dg;
     if (!desc || !canvas || !h_buffer || !params || !denoise || !state) return DG_ERR_INVALID_ARG;
     if (desc->h != h_buffer) return DG_ERR_INVALID_ARG;
@@ -823,6 +827,7 @@ extern "C" int dg_block_generate(const dg_head_desc* desc, int32_t n_blocks,
                                  float s_pad, int32_t* tokens_out, dg_canvas_state* states_out,
                                  void* workspace, size_t workspace_bytes, uint32_t* status,
                                  dg_stream_t stream) {
+    dg::NvtxRange nvtx_range("dg_block_generate");
     if (!desc || n_blocks < 0 || !y_blocks || !y_work || !canvas || !state || !h_buffer ||
         !params || !tokens_out || !states_out || desc->B < 1 || desc->S < 1)
         return DG_ERR_INVALID_ARG;
@@ -868,6 +873,7 @@ extern "C" int dg_nvfp4_scale_bytes(int32_t rows, int32_t d, size_t* bytes) {
 
 extern "C" int dg_nvfp4_pack_scales(const uint8_t* block_scales, int32_t rows, int32_t d,
                                     uint8_t* packed, dg_stream_t stream) {
+    dg::NvtxRange nvtx_range("dg_nvfp4_pack_scales");
     if (!block_scales || !packed || rows < 1 || d < 256 || d % 256 != 0)
         return DG_ERR_INVALID_ARG;
     if (dg::launch_pack_scales(block_scales, rows, d, packed,
@@ -879,6 +885,7 @@ extern "C" int dg_nvfp4_pack_scales(const uint8_t* block_scales, int32_t rows, i
 extern "C" int dg_quantize_nvfp4(const void* h_bf16, int32_t rows, int32_t d, uint8_t* codes,
                                  uint8_t* block_scale_packed, float* row_scale, uint32_t* status,
                                  dg_stream_t stream) {
+    dg::NvtxRange nvtx_range("dg_quantize_nvfp4");
     if (!h_bf16 || !codes || !block_scale_packed || !row_scale || rows < 1 || d < 256 ||
         d % 256 != 0)
         return DG_ERR_INVALID_ARG;

@@ -11,6 +11,7 @@
 #include <utility>
 
 #include "../../include/dgcanvas.h"
+#include "dg_nvtx.h"
 
 namespace {
 
@@ -117,6 +118,7 @@ int dg_canvas_step_host(const dg_head_desc* desc, const int32_t* canvas_in, int3
                         float* mean_entropy, int32_t keep_k, uint64_t seed, uint32_t pass,
                         dg_canvas_state* state, const dg_stop_rule* rule, void* workspace,
                         size_t workspace_bytes, uint32_t* status, dg_stream_t stream) {
+    dg::NvtxRange nvtx_range("dg_canvas_step_host");
     if (!desc || !desc->h || !canvas_in || !canvas_out || !workspace) return DG_ERR_INVALID_ARG;
     size_t base = 0;
     int rc = dg_workspace_bytes(desc, &base);

@@ -22,6 +22,7 @@
 #include <vector>
 
 #include "../../include/dgcanvas.h"
+#include "dg_nvtx.h"
 
 namespace {
 
@@ -54,6 +55,7 @@ extern "C" int dg_canvas_step_noalloc(const dg_head_desc* desc, const int32_t* c
                                       uint8_t* kept, float* mean_entropy, dg_canvas_state* state,
                                       const dg_stop_rule* rule, uint32_t* status,
                                       dg_stream_t stream) {
+    dg::NvtxRange nvtx_range("dg_canvas_step_noalloc");
     size_t need = 0;
     int rc = dg_workspace_bytes(desc, &need);
     if (rc != DG_OK) return rc;
