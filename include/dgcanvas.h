@@ -332,7 +332,9 @@ DG_API int dg_canvas_step_noalloc(const dg_head_desc* desc, const int32_t* canva
  * The device copies live in the workspace, in two staging sets used by successive calls in turn,
  * so the uploads of one call overlap the previous call's kernels; a set is not rewritten before
  * the pass that last used it has finished. Calls sharing a workspace must share `stream`. Not for
- * use under stream capture (DG_ERR_UNSUPPORTED): capture dg_canvas_step instead.
+ * use under stream capture (DG_ERR_UNSUPPORTED): capture dg_canvas_step instead. The library
+ * keeps one copy stream and four events per (workspace address, device) it has seen, for the
+ * life of the process.
  * dg_workspace_bytes_host: workspace bytes for this entry point (dg_workspace_bytes plus the two
  * staging sets).
  */
