@@ -28,7 +28,8 @@
  *
  * Conventions for every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller (for example PyTorch tensors),
- *     16-byte aligned. The library allocates no device memory on the step path: the caller
+ *     16-byte aligned; dg_canvas_step_host's hidden states and canvases are the one exception
+ *     (host memory). The library allocates no device memory on the step path: the caller
  *     passes a workspace of at least dg_workspace_bytes() bytes, 256-byte aligned.
  *   - `stream` is the caller's cudaStream_t (NULL = legacy default stream). Calls only enqueue
  *     work and never synchronise; results are valid once the stream reaches them.
