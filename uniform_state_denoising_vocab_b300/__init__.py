@@ -361,7 +361,7 @@ def dg_canvas_step(h, w, canvas_in, keep_k: int, seed: int, pass_: int, *, B: in
     return out
 
 
-def dg_canvas_loop(w, canvas, *, B: int, S: int, theta: float, y=None, denoise=None,
+def prepare_loop(w, canvas, *, B: int, S: int, theta: float, y=None, denoise=None,
                    h_buffer=None, w_scale=None, keep_k0: int = 32, keep_sched=None,
                    seed: int = 0, max_passes: int = 48, stable_passes: int = 2,
                    stop_mode: int = STOP_OR, start_pass: int = 0, init_random: bool = True,
@@ -369,8 +369,9 @@ def dg_canvas_loop(w, canvas, *, B: int, S: int, theta: float, y=None, denoise=N
                    trace: bool = False, timeline: bool = False, workspace=None, status=None,
                    outputs: dict | None = None, keep_rule: int = KEEP_CONFIDENCE,
                    mask_id: int | None = None, temp_start: float = 0.0, temp_end: float = 0.0,
-                   row_offset: int = 0, stream=None) -> dict:
-    """The whole denoising loop on the device (one graph launch, no host synchronisation).
+                   row_offset: int = 0) -> "PreparedLoop":
+    """Marshal the arguments of a dg_canvas_loop call once; PreparedLoop.run(stream) issues it
+    (again and again: the library reuses its captured graph while the arguments are unchanged).
 
     With y given (and denoise None) the built-in synthetic denoiser is used. `denoise`, if
     given, is a Python callable (canvas_ptr, pass_ptr, h_ptr, stream_handle) -> int that must
@@ -436,12 +437,29 @@ def dg_canvas_loop(w, canvas, *, B: int, S: int, theta: float, y=None, denoise=N
         fn = C.cast(cb, C.c_void_p)
         user = None
         keep += [cb]
-    rc = L.dg_canvas_loop(C.byref(desc), _ptr(canvas), _ptr(h_buffer), C.byref(params), fn, user,
-                          _ptr(state), _ptr(out["argmax"]), _ptr(out["conf"]),
-                          _ptr(out["entropy"]), _ptr(ws), ws.numel(), _ptr(st), _stream(stream))
-    _check(rc, "dg_canvas_loop")
+    call = (C.byref(desc), _ptr(canvas), _ptr(h_buffer), C.byref(params), fn, user, _ptr(state),
+            _ptr(out["argmax"]), _ptr(out["conf"]), _ptr(out["entropy"]), _ptr(ws), ws.numel(),
+            _ptr(st))
     out["_keepalive"] = keep + [ws, desc, params]
-    return out
+    return PreparedLoop(call, out)
+
+
+class PreparedLoop:
+    """One dg_canvas_loop call with its arguments marshalled (see prepare_loop)."""
+
+    def __init__(self, call, out):
+        self._call = call
+        self.out = out
+
+    def run(self, stream=None) -> dict:
+        _check(lib().dg_canvas_loop(*self._call, _stream(stream)), "dg_canvas_loop")
+        return self.out
+
+
+def dg_canvas_loop(w, canvas, *, stream=None, **kw) -> dict:
+    """The whole denoising loop on the device (one graph launch, no host synchronisation): the
+    keyword arguments of prepare_loop, issued once on `stream`."""
+    return prepare_loop(w, canvas, **kw).run(stream)
 
 
 def dg_block_generate(w, y_blocks, *, n_blocks: int, B: int, S: int, theta: float,
