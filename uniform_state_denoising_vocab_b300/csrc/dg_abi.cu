@@ -160,8 +160,10 @@ struct Layout {
 
 int layout_for(const dg_head_desc* d, int path, const DeviceInfo& di, Layout* L) {
     const int R = d->B * d->S;
-    if (path == PATH_SIMT)
+    if (path == PATH_SIMT) {
         L->plan = plan_head(R, d->V, d->d, kSimtBM, kSimtBN, di.sms * 8);
+        L->plan.parts = 2;  // two threads per row, one partial per half of each tile's columns
+    }
     else if (path == PATH_FP4 || path == PATH_FP4_QUANT) {
         L->plan = plan_head(R, d->V, d->d, kTcBM, kFp4BN, di.sms);  // single-CTA NVFP4 head
         L->plan.parts = 2;  // its epilogue keeps one state per half of the tile's columns

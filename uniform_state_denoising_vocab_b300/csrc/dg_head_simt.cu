@@ -2,9 +2,11 @@
 // epilogue as the tensor-core head. Used for fp32 operands, which the tensor cores would round
 // (tf32); it serves small heads (hidden size 64, vocabulary 4096 in the fp32 workload).
 //
-// One CTA of 128 threads per (row block, vocabulary group) unit: thread t owns slot row
-// mb*128 + t, keeps 32 hidden values of its row in registers, and accumulates 64 logits per
-// vocabulary tile against a 64 x 32 slice of W staged in shared memory (broadcast reads).
+// One CTA of 256 threads per (row block, vocabulary group) unit: threads t and t + 128 own slot
+// row mb*128 + t, each keeping 32 hidden values of the row in registers and accumulating its half
+// (32 logits) of every 64-column vocabulary tile against a 64 x 32 slice of W staged in shared
+// memory (broadcast reads); each half folds its columns into its own running state and writes
+// its own partial (two per row and unit).
 #include <cuda_runtime.h>
 
 #include "dg_common.cuh"
@@ -16,11 +18,15 @@ namespace {
 constexpr int BM = kSimtBM;  // 128 rows per CTA
 constexpr int BN = kSimtBN;  // 64 vocabulary columns per tile
 constexpr int KC = 32;       // hidden values per staging step
+constexpr int THREADS = 2 * BM;
+constexpr int HC = BN / 2;   // columns of a tile per thread
+static_assert(HC == 32, "one 32-column fold per thread and tile");
 
-__global__ void __launch_bounds__(BM)
+__global__ void __launch_bounds__(THREADS)
     head_simt_kernel(const float* __restrict__ h, const float* __restrict__ w, const HeadArgs args) {
     __shared__ __align__(16) float ws[BN][KC];
-    const int t = threadIdx.x;
+    const int t = threadIdx.x & (BM - 1);
+    const int half = threadIdx.x / BM;
     grid_dependency_wait();
     const int units = (args.stop != nullptr && *args.stop != 0) ? 0 : args.MB * args.n_groups;
     const int tl_pass = args.timeline != nullptr ? *args.pass_ptr : 0;
@@ -34,9 +40,9 @@ __global__ void __launch_bounds__(BM)
         const float crow = crow_base;
         RowState st = row_state_init();
         for (int nb = grp; nb < args.NT; nb += args.n_groups) {
-            float acc[BN];
+            float acc[HC];
 #pragma unroll
-            for (int j = 0; j < BN; ++j) acc[j] = 0.f;
+            for (int j = 0; j < HC; ++j) acc[j] = 0.f;
             for (int k0 = 0; k0 < args.d; k0 += KC) {
                 float hr[KC];
 #pragma unroll
@@ -45,15 +51,15 @@ __global__ void __launch_bounds__(BM)
                     hr[j] = (row_ok && k < args.d) ? h[static_cast<size_t>(row) * args.d + k] : 0.f;
                 }
                 __syncthreads();
-                for (int i = t; i < BN * KC; i += BM) {
+                for (int i = threadIdx.x; i < BN * KC; i += THREADS) {
                     const int n = nb * BN + i / KC, k = k0 + i % KC;
                     ws[i / KC][i % KC] =
                         (n < args.V && k < args.d) ? w[static_cast<size_t>(n) * args.d + k] : 0.f;
                 }
                 __syncthreads();
 #pragma unroll
-                for (int n = 0; n < BN; ++n) {
-                    const float4* wr = reinterpret_cast<const float4*>(ws[n]);
+                for (int n = 0; n < HC; ++n) {
+                    const float4* wr = reinterpret_cast<const float4*>(ws[half * HC + n]);
                     float a = acc[n];
 #pragma unroll
                     for (int q = 0; q < KC / 4; ++q) {
@@ -66,21 +72,16 @@ __global__ void __launch_bounds__(BM)
                     acc[n] = a;
                 }
             }
-            const int valid_tile = args.V - nb * BN;
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                float v[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = acc[c * 32 + j];
-                const int valid = valid_tile - c * 32;
-                if (valid >= 32)
-                    row_state_update<false>(st, v, crow, nb * BN + c * 32, 32);
-                else if (valid > 0)
-                    row_state_update<true>(st, v, crow, nb * BN + c * 32, valid);
-            }
+            const int n0 = nb * BN + half * HC;
+            const int valid = args.V - n0;
+            if (valid >= HC)
+                row_state_update<false>(st, acc, crow, n0, HC);
+            else if (valid > 0)
+                row_state_update<true>(st, acc, crow, n0, valid);
         }
         if (row_ok)
-            args.partials[static_cast<size_t>(row) * args.n_groups + grp] = pack(row_state_partial(st));
+            args.partials[static_cast<size_t>(row) * (2 * args.n_groups) + 2 * grp + half] =
+                pack(row_state_partial(st));
     }
     if (units > 0) timeline_end(args.timeline, tl_pass, DG_TL_HEAD);
 }
@@ -91,7 +92,7 @@ cudaError_t launch_head_simt(const float* h, const float* w, const HeadArgs& arg
                              cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(BM);
+    cfg.blockDim = dim3(THREADS);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     set_pdl_attr(&attr[0]);
