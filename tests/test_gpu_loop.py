@@ -143,6 +143,34 @@ def test_loop_graph_reuse_and_resume(dg):
         assert dg.state_fields(r3["state"])["passes"].tolist() == s1["passes"].tolist()
 
 
+def test_prepared_loop_reruns_match_fresh_calls(dg):
+    """prepare_loop marshals a loop call once; each run() is a whole loop from a fresh random
+    canvas, identical to a dg_canvas_loop call with the same arguments (same canvas, state and
+    statistics), run after run."""
+    from workloads import CONFIGS, make_loop_inputs
+    cfg = CONFIGS["loop_bf16_v32768_d256"]
+    x = make_loop_inputs(cfg)
+    tw = dev_bf16(x["w"], (cfg.V, cfg.d))
+    ty = dev(x["y"])
+    kw = dict(B=cfg.B, S=cfg.S, theta=cfg.theta, y=ty, keep_k0=cfg.keep_k, seed=cfg.seed,
+              max_passes=cfg.max_passes, n_content=cfg.n_content, s_content=cfg.s_content,
+              s_pad=cfg.s_pad)
+    c_ref = torch.empty(cfg.R, dtype=torch.int32, device="cuda")
+    ref = dg.dg_canvas_loop(tw, c_ref, **kw)
+    torch.cuda.synchronize()
+    c = torch.empty(cfg.R, dtype=torch.int32, device="cuda")
+    loop = dg.prepare_loop(tw, c, **kw)
+    for _ in range(3):
+        c.fill_(-1)
+        out = loop.run()
+        torch.cuda.synchronize()
+        assert torch.equal(c, c_ref)
+        assert torch.equal(out["state"], ref["state"])
+        for k in ("argmax", "conf", "entropy"):
+            assert torch.equal(out[k], ref[k]), k
+        assert int(out["status"][0]) == 0
+
+
 def test_loop_rules_on_device(dg):
     """Each stop rule fires at the expected pass on the device: cap with nothing kept, entropy
     at the first pass with large logits."""
