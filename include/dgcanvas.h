@@ -176,7 +176,13 @@ DG_API int dg_canvas_step(const dg_head_desc* desc, const int32_t* canvas_in, in
  * [B*S]) and the pass index (device int32 scalar) and writes the hidden states h_out (device,
  * [B*S, d] in the descriptor's h_dtype; BF16 when the head is E4M3 and h is quantised by the
  * library). It must be stream-ordered and capturable into a CUDA graph (no host sync, no
- * allocation). Return 0 on success.
+ * allocation): the library calls it while it captures the loop's graph, not once per pass, and
+ * the pass index is only known on the device. Return 0 on success.
+ * The captured graph is cached and replayed by later dg_canvas_loop calls whose arguments are
+ * all the same (the same hook function and `user` pointer included), without calling the hook
+ * again. So the work a hook enqueues for one (hook, user) must not change between such calls:
+ * the memory it reads may change in content, not in address. Pass a different `user` (or
+ * function) to have the loop captured afresh.
  */
 typedef int (*dg_denoise_fn)(void* user, const int32_t* canvas, const int32_t* pass,
                              void* h_out, dg_stream_t stream);
@@ -219,8 +225,8 @@ DG_API int dg_synth_denoise(void* user, const int32_t* canvas, const int32_t* pa
  *   state [B] (device): on entry `stable` is the resume count when start_pass > 0 (and is
  *     reset to 0 otherwise); on exit it holds passes/reason/mean_entropy per canvas.
  *   argmax/conf/entropy: optional device outputs of the last pass that ran.
- *   trace_mean_entropy [max_passes * B], trace_canvas [(max_passes + 1) * B*S] (the canvas
- *   entering pass p at row p; the final canvas after the last pass is not appended),
+ *   trace_mean_entropy [max_passes * B], trace_canvas [max_passes * B*S] (row p holds the
+ *   canvas entering pass p; the canvas left by the last pass is the `canvas` argument itself),
  *   trace_h [max_passes * B*S*d] (bytes of h_dtype), trace_argmax/conf/entropy
  *   [max_passes * B*S]: optional device traces of every pass, for checking.
  */
@@ -299,10 +305,10 @@ DG_API int dg_quantize_nvfp4(const void* h_bf16, int32_t rows, int32_t d, uint8_
 
 /*
  * dg_canvas_step without a caller-supplied workspace, for callers that cannot allocate device
- * memory: code running under CUDA graph stream capture (where cudaMalloc is not allowed), plugins
- * hosted by a framework that owns all device allocations, and latency-critical code that must not
- * risk the implicit synchronisation of cudaMalloc/cudaFree. (The pages describe no such entry
- * point; it has no counterpart in the method.)
+ * memory: plugins hosted by a framework that owns all device allocations, and latency-critical
+ * code that must not risk the implicit synchronisation of cudaMalloc/cudaFree or that runs under
+ * a device-memory budget fixed in advance. (The pages describe no such entry point; it has no
+ * counterpart in the method.)
  * Same arguments and results as dg_canvas_step minus the workspace. Its scratch is one array of
  * DG_NOALLOC_SCRATCH_BYTES compiled into the library (held by every GPU that loads it until the
  * process exits); descriptors needing more scratch than that (dg_workspace_bytes) are rejected

@@ -33,23 +33,54 @@ def test_algorithmic_work_of_the_quantised_heads():
 PEAKS = {"hbm_gbs": 6500.0, "bf16_tflops": 1700.0, "bf16_tflops_sustained": 1350.0}
 
 
-def test_roofline_compute_bound_bf16():
+def test_roofline_short_region_uses_the_burst_peak_and_is_hbm_bound():
+    """A 20-pass run (5 ms timed region at the maximum clock) is a kernel timed alone: the burst
+    tensor peak applies, so the bf16 pass is HBM-bound (t_mem 227 us > t_flop 222 us) and its
+    fraction is achieved GB/s over the copy bandwidth."""
     cfg = CONFIGS["pass_bf16_v262144_d2816"]
     flops, byts = bench.algorithmic(cfg)
-    head_us = 325.0
+    clocks = {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0}
+    regime = bench.tensor_regime(0.0054, clocks)
+    assert regime == "burst"
+    head_us = 263.3
+    r = {"head_ms": [head_us / 1e3] * 10, "flops": flops, "bytes": byts}
+    out = bench.roofline(cfg, r, PEAKS, "measured", step_s=270e-6, regime=regime)
+    assert out["bound"] == "hbm" and out["unit"] == "GB/s" and out["regime"] == "burst"
+    assert out["achieved"] == pytest.approx(byts / (head_us * 1e-6) / 1e9)
+    assert out["frac"] == pytest.approx(out["achieved"] / 6500.0) and out["frac"] < 1.0
+    assert out["t_roof_us"] == pytest.approx(byts / 6.5e12 * 1e6)
+    assert out["roof_frac"] == pytest.approx(out["frac"])
+    assert out["kernel_launches_timed"] == 10
+    # datasheet roofline: max(bytes / 8 TB/s, flops / 2.25 PF/s) = the HBM term (184.7 us)
+    assert out["datasheet_roof_frac"] == pytest.approx(byts / 8e12 / (head_us * 1e-6))
+    assert out["kernel"] == "head_tc2_kernel<0>"
+
+
+def test_tensor_regime_rule():
+    # seconds-long run at a power-capped clock: the sustained rate
+    assert bench.tensor_regime(2.0, {"sm_mhz": 1160.0, "sm_max_mhz": 2032.0}) == "sustained"
+    # seconds-long run that kept the clock near its maximum: burst
+    assert bench.tensor_regime(2.0, {"sm_mhz": 2000.0, "sm_max_mhz": 2032.0}) == "burst"
+    # short region, whatever the clock: burst
+    assert bench.tensor_regime(0.3, {"sm_mhz": 1160.0, "sm_max_mhz": 2032.0}) == "burst"
+    # no clock samples: decided by the region's length
+    assert bench.tensor_regime(2.0, {"sm_mhz": None, "sm_max_mhz": None}) == "sustained"
+
+
+def test_roofline_sustained_regime_compute_bound_bf16():
+    cfg = CONFIGS["pass_bf16_v262144_d2816"]
+    flops, byts = bench.algorithmic(cfg)
+    head_us = 340.0
     r = {"head_ms": [head_us / 1e3] * 4, "flops": flops, "bytes": byts}
-    out = bench.roofline(cfg, r, PEAKS, "measured", step_s=337e-6)
+    out = bench.roofline(cfg, r, PEAKS, "measured", step_s=350e-6, regime="sustained")
     # t_flop = 3.78e11 / 1.35e15 = 280 us > t_mem = 1.478e9 / 6.5e12 = 227 us: tensor-bound
     assert out["bound"] == "tensor" and out["unit"] == "TFLOP/s"
     assert out["achieved"] == pytest.approx(flops / (head_us * 1e-6) / 1e12)
     assert out["peak"] == 1350.0
-    assert out["frac"] == pytest.approx(out["achieved"] / 1350.0)
+    assert out["frac"] == pytest.approx(out["achieved"] / 1350.0) and out["frac"] < 1.0
     assert out["t_roof_us"] == pytest.approx(flops / 1.35e15 * 1e6)
     assert out["hbm_frac"] == pytest.approx(byts / (head_us * 1e-6) / 6.5e12)
-    assert out["step_roof_frac"] == pytest.approx(flops / 1.35e15 / 337e-6)
-    # datasheet roofline: max(bytes / 8 TB/s, flops / 2.25 PF/s) = the HBM term (184.7 us)
-    assert out["datasheet_roof_frac"] == pytest.approx(byts / 8e12 / (head_us * 1e-6))
-    assert out["kernel"] == "head_tc2_kernel<0>"
+    assert out["step_roof_frac"] == pytest.approx(flops / 1.35e15 / 350e-6)
 
 
 def test_roofline_memory_bound_nvfp4_uses_the_hbm_peak():
@@ -57,7 +88,7 @@ def test_roofline_memory_bound_nvfp4_uses_the_hbm_peak():
     flops, byts = bench.algorithmic(cfg)
     r = {"head_ms": [0.1175], "flops": flops, "bytes": byts}
     out = bench.roofline(cfg, r, PEAKS, "measured", step_s=130e-6)
-    # t_flop at 6 x 1.35 PF/s = 47 us < t_mem = 64 us: HBM-bound
+    # t_flop at 6 x 1.7 PF/s = 37 us < t_mem = 64 us: HBM-bound
     assert out["bound"] == "hbm" and out["unit"] == "GB/s"
     assert out["achieved"] == pytest.approx(byts / 117.5e-6 / 1e9)
     assert out["frac"] == pytest.approx(out["achieved"] / 6500.0)
@@ -71,6 +102,31 @@ def test_roofline_e4m3_doubles_the_tensor_peak():
     out = bench.roofline(cfg, r, PEAKS, "measured", step_s=160e-6)
     assert out["tensor_frac_sustained"] == pytest.approx(flops / 150e-6 / 2.7e15)
     assert out["tensor_frac_burst"] == pytest.approx(flops / 150e-6 / 3.4e15)
+
+
+def test_roofline_fp32_head_is_bounded_by_the_cuda_cores():
+    cfg = CONFIGS["pass_f32_v4096_d64"]
+    flops, byts = bench.algorithmic(cfg)
+    r = {"head_ms": [0.020], "flops": flops, "bytes": byts}
+    out = bench.roofline(cfg, r, PEAKS, "measured", step_s=25e-6)
+    alu = 148 * 128 * 2 * 2.032e9 / 1e12
+    # t_flop = 1.34e8 / 77 TF/s = 1.7 us > t_mem = 1.05 MB / 6.5 TB/s = 0.16 us
+    assert out["bound"] == "alu" and out["peak"] == pytest.approx(alu)
+    assert out["frac"] == pytest.approx(flops / 20e-6 / 1e12 / alu)
+
+
+def test_clock_summary_window_and_bracketing():
+    clk = bench.ClockSampler(0)
+    # (t, sm_mhz, sm_max_mhz, reasons mask, power W): power cap (0x4) active at t=1.0
+    clk.rows = [(0.0, 2032, 2032, 0, 300.0), (1.0, 1200, 2032, 0x4, 1100.0),
+                (1.5, 1180, 2032, 0x4, 1100.0), (3.0, 2032, 2032, 0, 250.0)]
+    s = clk.summary(0.9, 1.6)
+    assert s["sm_mhz"] == 1190 and s["samples"] == 2 and s["reasons"] == ["sw_power_cap"]
+    assert s["window"] == "timed region"
+    # a window shorter than the sampling period: the samples bracketing it
+    s = clk.summary(2.0, 2.1)
+    assert s["samples"] == 2 and s["sm_mhz"] == (1180 + 2032) / 2
+    assert s["window"].startswith("timed region and")
 
 
 def test_loop_breakdown_from_a_timeline():

@@ -1,16 +1,16 @@
 """dg_canvas_step_noalloc: the canvas pass for callers that cannot allocate device memory
-(graph-capture regions, framework-hosted plugins, code that must not risk cudaMalloc's implicit
-synchronisation). Its scratch is an array compiled into the library, so the caller passes only
-inputs and outputs. Checked through the C ABI against the workspace-taking dg_canvas_step on
-two different calls in a row (so a stale scratch from the first call would show in the second).
-This file is collected last on purpose."""
+(plugins whose host framework owns every device allocation, code that must not risk
+cudaMalloc's implicit synchronisation or that runs under a fixed device-memory budget). Its
+scratch is an array compiled into the library, so the caller passes only inputs and outputs.
+Checked through the C ABI against the workspace-taking dg_canvas_step on two different calls in
+a row (so a stale scratch from the first call would show in the second): both entry points run
+the same kernels on the same inputs, so every output must be bit-identical. This file is
+collected last on purpose."""
 import ctypes as C
 
 import numpy as np
 import pytest
 import torch
-
-from parity import TOL
 
 pytestmark = pytest.mark.gpu
 
@@ -68,10 +68,27 @@ def test_noalloc_matches_workspace_step_on_two_calls(dg):
     torch.cuda.synchronize()
     for g, r in zip(got, ref):
         assert int(g["status"][0]) == 0
-        for k in ("canvas", "argmax", "kept"):
+        for k in ("canvas", "argmax", "kept", "conf", "entropy", "mean_entropy"):
             assert torch.equal(g[k], r[k]), k
-        for k in ("conf", "entropy", "mean_entropy"):
-            assert torch.allclose(g[k], r[k], atol=TOL["bf16"], rtol=0), k
+
+
+def test_noalloc_largest_workload_shape_that_fits(dg):
+    """Eight 256-slot canvases (2048 rows, the batched workload's row count) with a vocabulary
+    wide enough that the head splits it into as many groups as at V = 262144: the softmax
+    partials take about 1.2 MB of the 4 MiB array (with 74 CTA pairs). Two calls in a row,
+    bit-identical to dg_canvas_step."""
+    B, S, V, d = 8, 256, 40000, 64
+    h, w, c = _case(B, S, V, d, 13)
+    desc = dg.make_desc(h, w, B=B, S=S)
+    need = dg.dg_workspace_bytes(desc)
+    assert need <= (4 << 20), need
+    for seed, p in ((2, 0), (3, 1)):
+        g = _noalloc(dg, h, w, c, B, S, 32, seed, p)
+        r = dg.dg_canvas_step(h, w, c, 32, seed, p, B=B, S=S)
+        torch.cuda.synchronize()
+        assert int(g["status"][0]) == 0
+        for k in ("canvas", "argmax", "kept", "conf", "entropy", "mean_entropy"):
+            assert torch.equal(g[k], r[k]), k
 
 
 def test_noalloc_rejects_descriptors_beyond_its_scratch(dg):

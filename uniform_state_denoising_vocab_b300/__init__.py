@@ -12,6 +12,7 @@ dg_canvas_loop (plus dg_synth_denoise as the built-in denoiser hook).
 from __future__ import annotations
 
 import ctypes as C
+import itertools
 from pathlib import Path
 
 import torch
@@ -75,6 +76,8 @@ class SynthParams(C.Structure):
     _fields_ = [("desc", C.POINTER(HeadDesc)), ("y", C.c_void_p), ("n_content", C.c_int32),
                 ("s_content", C.c_float), ("s_pad", C.c_float), ("status", C.c_void_p)]
 
+
+_HOOK_TOKENS = itertools.count(1)
 
 DENOISE_FN = C.CFUNCTYPE(C.c_int, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p)
 
@@ -375,7 +378,8 @@ def prepare_loop(w, canvas, *, B: int, S: int, theta: float, y=None, denoise=Non
 
     With y given (and denoise None) the built-in synthetic denoiser is used. `denoise`, if
     given, is a Python callable (canvas_ptr, pass_ptr, h_ptr, stream_handle) -> int that must
-    enqueue capturable work on the stream it receives. `outputs` may hold preallocated
+    enqueue capturable work on the stream it receives; it is called while the library captures
+    the loop (once per prepared call, on its first run), and later runs replay that work. `outputs` may hold preallocated
     argmax/conf/entropy tensors [B*S]; with the same tensors (and the same other arguments) a
     repeated call reuses the captured graph. With timeline=True the result holds
     "trace_timeline" [max_passes, 3, 2] (uint64 stored as int64): per pass, the device global
@@ -435,7 +439,9 @@ def prepare_loop(w, canvas, *, B: int, S: int, theta: float, y=None, denoise=Non
     else:
         cb = DENOISE_FN(lambda u, c, p, h, s: int(denoise(c, p, h, s) or 0))
         fn = C.cast(cb, C.c_void_p)
-        user = None
+        # The library caches the captured loop per (hook, user): a fresh token per prepared call
+        # keeps a later callback whose trampoline reuses a freed address from replaying this one.
+        user = C.c_void_p(next(_HOOK_TOKENS))
         keep += [cb]
     call = (C.byref(desc), _ptr(canvas), _ptr(h_buffer), C.byref(params), fn, user, _ptr(state),
             _ptr(out["argmax"]), _ptr(out["conf"]), _ptr(out["entropy"]), _ptr(ws), ws.numel(),

@@ -7,6 +7,8 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <set>
+#include <tuple>
 #include <vector>
 
 #include "../../include/dgcanvas.h"
@@ -14,6 +16,20 @@
 #include "dg_internal.h"
 
 namespace dg {
+
+cudaError_t ensure_smem_attr(const void* fn, int bytes) {
+    static std::mutex mu;
+    static std::set<std::tuple<int, const void*, int>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    const auto key = std::make_tuple(dev, fn, bytes);
+    if (done.count(key)) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.insert(key);
+    return e;
+}
 
 HeadPlan plan_head(int R, int V, int d, int BM, int BN, int slots) {
     HeadPlan p{};
@@ -781,11 +797,12 @@ extern "C" int dg_canvas_loop(const dg_head_desc* desc, int32_t* canvas, void* h
 
     std::lock_guard<std::mutex> lk(g_loop_mu);
     LoopEntry* E = nullptr;
-    // A user-supplied denoiser may read state behind `user` when it is captured, so only the
-    // built-in denoiser (whose parameters are part of the key) reuses a captured graph.
-    if (denoise == dg_synth_denoise)
-        for (LoopEntry* e : g_loops)
-            if (same_key(e->key, key)) E = e;
+    // A captured graph is reused whenever every argument matches: the built-in denoiser's
+    // parameters by value, a caller's denoiser by (function, user) pointer. A caller's hook is
+    // therefore only invoked while a new graph is captured; the header states that the work it
+    // enqueues must not change between calls with the same arguments.
+    for (LoopEntry* e : g_loops)
+        if (same_key(e->key, key)) E = e;
     if (!E) {
         E = new LoopEntry();
         E->key = key;
@@ -814,10 +831,6 @@ extern "C" int dg_canvas_loop(const dg_head_desc* desc, int32_t* canvas, void* h
         return DG_ERR_CUDA;
     if (cudaGraphLaunch(E->exec, st) != cudaSuccess) return DG_ERR_CUDA;
     if (cudaEventRecord(E->done, st) != cudaSuccess) return DG_ERR_CUDA;
-    if (denoise != dg_synth_denoise) {
-        // not reusable: keep it until its launch has finished, then let eviction drop it
-        E->stamp = 0;
-    }
     evict_finished_locked();
     return DG_OK;
 }

@@ -292,13 +292,9 @@ cudaError_t launch_head_fp4(const void* qh, const uint8_t* sfa, const void* qw, 
     if (!make_map_u8(&ma, qh, args.R, args.d / 2, BM) ||
         !make_map_u8(&mb, qw, args.V, args.d / 2, BN))
         return cudaErrorInvalidValue;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(head_fp4_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    if (cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(head_fp4_kernel), SMEM_BYTES);
+        e != cudaSuccess)
+        return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kFp4Threads);

@@ -279,15 +279,9 @@ cudaError_t launch_head_tc(int kind, const void* h, const void* w, const HeadArg
         !make_map(&mb, w, eb, args.V, args.d, plan.pair ? BN / 2 : BN))
         return cudaErrorInvalidValue;
     if (plan.pair) return launch_head_tc2(kind, ma, mb, args, plan.grid, stream);
-    static bool attr_set[2] = {false, false};
     const void* fn = kind == 0 ? reinterpret_cast<const void*>(head_tc_kernel<0>)
                                : reinterpret_cast<const void*>(head_tc_kernel<1>);
-    if (!attr_set[kind]) {
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set[kind] = true;
-    }
+    if (cudaError_t ea = ensure_smem_attr(fn, SMEM_BYTES); ea != cudaSuccess) return ea;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.grid);
     cfg.blockDim = dim3(kTcThreads);

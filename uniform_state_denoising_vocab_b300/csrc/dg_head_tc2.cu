@@ -254,15 +254,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 cudaError_t launch_head_tc2(int kind, const CUtensorMap& ma, const CUtensorMap& mb,
                             const HeadArgs& args, int n_pairs, cudaStream_t stream) {
-    static bool attr_set[2] = {false, false};
     const void* fn = kind == 0 ? reinterpret_cast<const void*>(head_tc2_kernel<0>)
                                : reinterpret_cast<const void*>(head_tc2_kernel<1>);
-    if (!attr_set[kind]) {
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set[kind] = true;
-    }
+    cudaError_t e = ensure_smem_attr(fn, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * n_pairs);
     cfg.blockDim = dim3(kTcThreads);
@@ -288,8 +283,8 @@ int head_tc2_max_pairs() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
     if (cached[dev] > 0) return cached[dev];
-    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(head_tc2_kernel<0>),
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
+    if (ensure_smem_attr(reinterpret_cast<const void*>(head_tc2_kernel<0>), SMEM_BYTES) !=
+        cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2);

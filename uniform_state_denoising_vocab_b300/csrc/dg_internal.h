@@ -109,6 +109,11 @@ inline void set_pdl_attr(cudaLaunchAttribute* a) {
     a->val.programmaticStreamSerializationAllowed = 1;
 }
 
+// Opts kernel `fn` in to `bytes` of dynamic shared memory on the current device, once per
+// (device, kernel, size). The attribute belongs to the device's context, so a process that
+// drives several GPUs sets it on each; thread-safe.
+cudaError_t ensure_smem_attr(const void* fn, int bytes);
+
 // Tensor-core head (bf16: kind = 0, e4m3: kind = 1). h and w are device row-major matrices.
 // Runs the CTA-pair kernel when plan.pair, else the single-CTA kernel.
 cudaError_t launch_head_tc(int kind, const void* h, const void* w, const HeadArgs& args,

@@ -1,13 +1,16 @@
 // dg_noalloc.cu -- dg_canvas_step_noalloc: one canvas pass whose scratch memory is a fixed
 // array compiled into the library, for callers that cannot allocate device memory.
 //
-// Who cannot allocate: code running while a stream is being captured into a CUDA graph
-// (cudaMalloc is not a capturable operation), plugins and custom operators hosted by a
-// framework that owns every device allocation and forbids its extensions from calling the CUDA
-// allocator, and latency-critical callers that must never risk the implicit device
-// synchronisation cudaMalloc/cudaFree can cause. They pass only inputs and outputs; the
-// softmax partials (and, for an E4M3 head fed bf16 hidden states, the quantised copy of h)
-// live in `g_scratch` below.
+// Who cannot allocate: plugins and custom operators hosted by a framework that owns every
+// device allocation and forbids its extensions from calling the CUDA allocator, and
+// latency-critical callers that must never risk the implicit device synchronisation that
+// cudaMalloc/cudaFree can cause, or that run under a fixed device-memory budget set before they
+// start. They pass only inputs and outputs; the softmax partials (and, for an E4M3 head fed
+// bf16 hidden states, the quantised copy of h) live in `g_scratch` below.
+//
+// Set-up: the first call on each device looks up the array's device address with
+// cudaGetSymbolAddress (with that device current) and caches it; make that first call before
+// any stream capture.
 //
 // Sharing rules: every call in the process on the same device uses the same array, and the
 // array keeps the previous call's contents. Each pass fully rewrites every scratch byte it
