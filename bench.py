@@ -73,23 +73,51 @@ REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0
                "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
 
-def _nvml_handle(pynvml, dev_index: int):
-    """NVML handle of the CUDA device `dev_index` (matched by UUID, then PCI id, then index)."""
-    props = torch.cuda.get_device_properties(dev_index)
-    try:
-        return pynvml.nvmlDeviceGetHandleByUUID("GPU-" + str(props.uuid))
-    except Exception:
-        pass
-    try:
-        bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
-        return pynvml.nvmlDeviceGetHandleByPciBusId(bus)
-    except Exception:
-        return pynvml.nvmlDeviceGetHandleByIndex(dev_index)
+class Nvml:
+    """The few read-only NVML queries the clock sampler needs, through ctypes on the driver's
+    libnvidia-ml.so.1 (no Python NVML package is required)."""
+    CLOCK_SM = 1
+
+    def __init__(self, dev_index: int):
+        import ctypes as C
+        self.C = C
+        self.lib = C.CDLL("libnvidia-ml.so.1")
+        init = getattr(self.lib, "nvmlInit_v2", None) or self.lib.nvmlInit
+        self._ok(init())
+        self.h = C.c_void_p()
+        props = torch.cuda.get_device_properties(dev_index)
+        rc = self.lib.nvmlDeviceGetHandleByUUID(("GPU-" + str(props.uuid)).encode(),
+                                                C.byref(self.h))
+        if rc != 0:
+            bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+            f = getattr(self.lib, "nvmlDeviceGetHandleByPciBusId_v2", None) or \
+                self.lib.nvmlDeviceGetHandleByPciBusId
+            self._ok(f(bus.encode(), C.byref(self.h)))
+        self._reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    @staticmethod
+    def _ok(rc):
+        if rc != 0:
+            raise RuntimeError(f"NVML error {rc}")
+
+    def max_sm_mhz(self) -> int:
+        v = self.C.c_uint()
+        self._ok(self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, self.C.byref(v)))
+        return v.value
+
+    def sample(self, mx: int):
+        C = self.C
+        sm, rs, mw = C.c_uint(), C.c_ulonglong(), C.c_uint()
+        self._ok(self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, C.byref(sm)))
+        self._ok(self._reasons(self.h, C.byref(rs)))
+        self._ok(self.lib.nvmlDeviceGetPowerUsage(self.h, C.byref(mw)))
+        return (time.perf_counter(), sm.value, mx, rs.value, mw.value / 1e3)
 
 
 class ClockSampler:
     """Samples the SM clock, its maximum, the clock-event reasons and the power draw every
-    `period_s` from a background thread with read-only NVML queries, for the whole life of the
+    `period_s` from a background thread with read-only NVML queries (Nvml), for the whole life of the
     `with` block (warm-up, timed and end-to-end legs), so that even a timed region of a few
     milliseconds has samples around it. mark() stamps host times; summary(t0, t1) reports the
     samples taken between two stamps (or, if the window is shorter than the sampling period,
@@ -105,12 +133,9 @@ class ClockSampler:
     def __enter__(self):
         import threading
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            h = _nvml_handle(pynvml, self.dev_index)
-            get_reasons = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons",
-                                  getattr(pynvml, "nvmlDeviceGetCurrentClocksThrottleReasons", None))
-            mx = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+            nv = Nvml(self.dev_index)
+            mx = nv.max_sm_mhz()
+            self.rows.append(nv.sample(mx))
         except Exception as e:     # no NVML: report why instead of clocks
             self.error = f"NVML unavailable: {e!r}"[:200]
             return self
@@ -119,9 +144,7 @@ class ClockSampler:
         def poll():
             while not self._stop.is_set():
                 try:
-                    self.rows.append((time.perf_counter(),
-                                      pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM), mx,
-                                      int(get_reasons(h)), pynvml.nvmlDeviceGetPowerUsage(h) / 1e3))
+                    self.rows.append(nv.sample(mx))
                 except Exception as e:
                     self.error = repr(e)[:200]
                     return

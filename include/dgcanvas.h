@@ -228,7 +228,9 @@ DG_API int dg_synth_denoise(void* user, const int32_t* canvas, const int32_t* pa
  *   trace_mean_entropy [max_passes * B], trace_canvas [max_passes * B*S] (row p holds the
  *   canvas entering pass p; the canvas left by the last pass is the `canvas` argument itself),
  *   trace_h [max_passes * B*S*d] (bytes of h_dtype), trace_argmax/conf/entropy
- *   [max_passes * B*S]: optional device traces of every pass, for checking.
+ *   [max_passes * B*S]: optional device traces of every pass, for checking. Rows of passes
+ *   that did not run are left as they were; so are a stopped canvas's statistics and mean
+ *   entropy in later passes, while its canvas trace keeps showing its frozen canvas.
  */
 typedef struct {
     dg_stop_rule rule;

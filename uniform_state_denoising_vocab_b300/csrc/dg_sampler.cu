@@ -303,8 +303,12 @@ __global__ void __cluster_dims__(kMergeCluster, 1, 1) __maxnreg__(40)
         }
     }
 
-    if (frozen && a.canvas_out && a.canvas_out != a.canvas_in && tid < nrows)
-        a.canvas_out[base + j0 + tid] = old_tok;
+    if (frozen && a.canvas_out && tid < nrows) {
+        const int r = base + j0 + tid;
+        if (a.canvas_out != a.canvas_in) a.canvas_out[r] = old_tok;
+        // a stopped canvas enters every later pass unchanged: its canvas trace says so
+        if (a.trace_canvas && a.ctl) a.trace_canvas[static_cast<size_t>(p) * a.R + r] = old_tok;
+    }
 
     // loop mode: the last canvas of the pass advances the pass and sets the graph condition
     if (a.ctl && c == 0 && tid == 0) {
