@@ -291,6 +291,9 @@ def roofline(cfg, r, peaks, peak_kind, step_s, regime="burst"):
                      else {"bf16": "head_tc_kernel<0>", "e4m3": "head_tc_kernel<1>"}[cfg.precision])
     out["kernel_us"] = head_s * 1e6
     out["kernel_launches_timed"] = len(r["head_ms"])
+    if r.get("head_clock"):
+        out["kernel_sm_mhz_effective"] = r["head_clock"]["sm_mhz_effective"]
+        out["kernel_kcycles"] = r["head_clock"]["head_kcycles"]
     out["t_roof_us"] = max(t_mem, t_flop) * 1e6
     out["roof_frac"] = max(t_mem, t_flop) / head_s
     out["hbm_frac"] = r["bytes"] / head_s / 1e9 / peaks["hbm_gbs"]
@@ -413,6 +416,8 @@ def run_pass(cfg, steps, warmup, ws_, clk, e2e_steps=0):
     sample = max(1, min(8, steps // 8))
     heads = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
              for _ in range(0, steps, sample)]
+    # each bracketed head also writes its SM clock sample (clock64 and global timer in CTA 0)
+    clk_samples = torch.zeros(len(heads), 4, dtype=torch.int64, device=dev)
     for a_, b_ in heads:    # create the event handles outside the timed region
         a_.record(stream)
         b_.record(stream)
@@ -424,6 +429,7 @@ def run_pass(cfg, steps, warmup, ws_, clk, e2e_steps=0):
     for i in range(steps):
         if i % sample == sample - 1:
             dg.dg_profile_next_head(*heads[i // sample])
+            dg.dg_profile_next_head_clock(clk_samples[i // sample])
         step(warmup + i, canvas if i % 2 == 0 else canvas_out, canvas_out if i % 2 == 0 else canvas)
     ev1.record(stream)
     torch.cuda.synchronize()
@@ -432,6 +438,7 @@ def run_pass(cfg, steps, warmup, ws_, clk, e2e_steps=0):
     t_ms = ev0.elapsed_time(ev1)
     head_ms = [a.elapsed_time(b) for a, b in heads[: steps // sample]]
     out = {"t_s": t_ms / 1e3, "units": cfg.B * steps, "head_ms": head_ms,
+           "head_clock": dg.sm_clock_stats(clk_samples[: steps // sample]),
            "clocks": clk.summary(t0, t1), "status": int(status.item()),
            "launches": launches_per_step * steps, "flops": flops, "bytes": byts}
     if e2e_steps:
@@ -548,20 +555,28 @@ def run_loop(cfg, steps, warmup, ws_, clk, e2e_steps=0):
     sm = torch.empty(cfg.B, device=dev)
     heads = []
     n_head = max(20, min(400, steps * passes_per_loop))
+    clk_samples = torch.zeros(n_head, 4, dtype=torch.int64, device=dev)
     for i in range(n_head):
         ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
         dg.dg_profile_next_head(*ev)
+        dg.dg_profile_next_head_clock(clk_samples[i])
         _launch_checked(L.dg_canvas_stats(C.byref(desc), P(sa), P(sc), P(se), P(sm), P(wsb),
                                           wsb.numel(), P(status),
                                           C.c_void_p(stream.cuda_stream)), dg)
         heads.append(ev)
     torch.cuda.synchronize()
     out["head_ms"] = [a.elapsed_time(b) for a, b in heads[len(heads) // 4:]]
-    # in-graph breakdown of one more (untimed) loop from the library's per-pass kernel timeline
-    rt = dg.dg_canvas_loop(w, canvas, timeline=True, **kw)
+    out["head_clock"] = dg.sm_clock_stats(clk_samples[len(heads) // 4:])
+    # in-graph breakdown of one more (untimed) loop from the library's per-pass kernel timeline,
+    # with each pass's head clock sample (effective SM clock, head cycles)
+    rt = dg.dg_canvas_loop(w, canvas, timeline=True, sm_clock=True, **kw)
     torch.cuda.synchronize()
+    npass = int(dg.state_fields(rt["state"])["passes"].max())
     out["loop_breakdown_us"] = loop_breakdown(dg.timeline_us(rt["trace_timeline"], cfg.max_passes),
-                                              int(dg.state_fields(rt["state"])["passes"].max()))
+                                              npass)
+    hc = dg.sm_clock_stats(rt["trace_sm_clock"][:npass])
+    out["loop_breakdown_us"]["head_sm_mhz_effective"] = hc["sm_mhz_effective"]
+    out["loop_breakdown_us"]["head_kcycles"] = hc["head_kcycles"]
     return out
 
 

@@ -253,6 +253,10 @@ typedef struct {
     unsigned long long* trace_timeline;
     float temp_start, temp_end;  /* temperature schedule; temp_start = 0: none */
     uint64_t row_offset;         /* added to the row index of every re-draw key */
+    /* optional device [max_passes * 4] uint64: per pass p, the SM clock sample of its head
+       kernel (see dg_profile_next_head_clock) at index p * 4; rows of passes that did not run
+       stay as they were. */
+    unsigned long long* trace_sm_clock;
 } dg_loop_params;
 
 /* Kernels recorded in dg_loop_params.trace_timeline. */
@@ -361,6 +365,17 @@ DG_API int dg_canvas_step_host(const dg_head_desc* desc, const int32_t* canvas_i
  * are being captured into a graph do not consume it. Passing NULLs clears a pending request.
  */
 DG_API int dg_profile_next_head(void* start_event, void* stop_event);
+
+/*
+ * Instrumentation: make the next dg_canvas_stats / dg_canvas_step call issued by this host
+ * thread (not being captured) have its vocabulary-head kernel write an SM clock sample to
+ * clock_sample (device, 4 x uint64, 8-byte aligned): CTA 0's clock64 counter and the global
+ * timer (ns) when it got past its wait on the previous kernel, then the same two when it
+ * finished. (cycles / ns) is the SM clock the kernel ran at, and the cycle count its duration
+ * independent of that clock. One-shot; NULL clears a pending request. Independent of
+ * dg_profile_next_head; both may be pending for the same call.
+ */
+DG_API int dg_profile_next_head_clock(unsigned long long* clock_sample);
 
 /* Human-readable name of a DG_ERR_* code or DG_ST_* bit set. */
 DG_API const char* dg_status_string(int code);

@@ -54,6 +54,7 @@ int main(void) {
   P(dg_loop_params, keep_sched) P(dg_loop_params, seed) P(dg_loop_params, start_pass)
   P(dg_loop_params, trace_h) P(dg_loop_params, trace_entropy) P(dg_loop_params, trace_timeline)
   P(dg_loop_params, temp_start) P(dg_loop_params, temp_end) P(dg_loop_params, row_offset)
+  P(dg_loop_params, trace_sm_clock)
   P(dg_stop_rule, keep_rule) P(dg_stop_rule, redraw_mode) P(dg_stop_rule, mask_id)
   printf("dg_synth_params %zu\n", sizeof(dg_synth_params));
   P(dg_synth_params, n_content) P(dg_synth_params, s_pad) P(dg_synth_params, status)

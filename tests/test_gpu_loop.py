@@ -403,9 +403,22 @@ def test_loop_timeline_trace(dg):
     c0 = torch.empty(cfg.R, dtype=torch.int32, device="cuda")
     r0 = dg.dg_canvas_loop(tw, c0, **kw)
     c1 = torch.empty(cfg.R, dtype=torch.int32, device="cuda")
-    r1 = dg.dg_canvas_loop(tw, c1, timeline=True, **kw)
+    r1 = dg.dg_canvas_loop(tw, c1, timeline=True, sm_clock=True, **kw)
     torch.cuda.synchronize()
     assert torch.equal(c0, c1)
+    # each pass that ran has its head's SM clock sample: ordered stamps, a plausible clock, and
+    # a global-timer span inside the head's timeline interval; later rows stay zero
+    P_ = int(dg.state_fields(r1["state"])["passes"][0])
+    ck = host(r1["trace_sm_clock"]).view(np.uint64).astype(np.float64)
+    tlr = host(r1["trace_timeline"]).view(np.uint64).reshape(cfg.max_passes, 3, 2)
+    for p in range(P_):
+        assert ck[p, 2] > ck[p, 0] and ck[p, 3] > ck[p, 1], p
+        mhz = (ck[p, 2] - ck[p, 0]) / (ck[p, 3] - ck[p, 1]) * 1e3
+        assert 200.0 < mhz < 2500.0, (p, mhz)
+        assert tlr[p, 1, 0] <= ck[p, 1] and ck[p, 3] <= tlr[p, 1, 1], p
+    assert (ck[P_:] == 0).all()
+    st = dg.sm_clock_stats(r1["trace_sm_clock"][:P_])
+    assert st["samples"] == P_ and st["head_kcycles"] > 0
     P = int(dg.state_fields(r1["state"])["passes"][0])
     tl = dg.timeline_us(r1["trace_timeline"], cfg.max_passes)
     prev_end = -1.0

@@ -147,6 +147,28 @@ def test_in_place_and_stats_entry_agree(dg, orc):
         assert torch.equal(r1[k], st[k]) and torch.equal(r1[k], r2[k])
 
 
+def test_head_clock_sample_is_one_shot(dg):
+    """dg_profile_next_head_clock: the next stats call's head writes a plausible SM clock
+    sample, later calls leave it alone, and the results are those of an uninstrumented call."""
+    B, S, V, d = 1, 256, 20000, 512
+    h, w, canvas = _rand_case(B, S, V, d, 6, "bf16")
+    th, tw = dev_bf16(_bits(h), (B * S, d)), dev_bf16(_bits(w), (V, d))
+    ref = dg.dg_canvas_stats(th, tw, B=B, S=S)
+    smp = torch.zeros(4, dtype=torch.int64, device="cuda")
+    dg.dg_profile_next_head_clock(smp)
+    a = dg.dg_canvas_stats(th, tw, B=B, S=S)
+    torch.cuda.synchronize()
+    first = smp.clone()
+    b = dg.dg_canvas_stats(th, tw, B=B, S=S)
+    torch.cuda.synchronize()
+    assert torch.equal(smp, first)
+    c = host(first).view(np.uint64).astype(np.float64)
+    assert c[2] > c[0] and c[3] > c[1]
+    assert 200.0 < (c[2] - c[0]) / (c[3] - c[1]) * 1e3 < 2500.0
+    for k in ("argmax", "conf", "entropy", "mean_entropy"):
+        assert torch.equal(a[k], ref[k]) and torch.equal(b[k], ref[k]), k
+
+
 def test_deterministic(dg):
     B, S, V, d = 2, 256, 20000, 512
     h, w, canvas = _rand_case(B, S, V, d, 4, "bf16")

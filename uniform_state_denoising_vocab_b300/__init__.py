@@ -23,7 +23,8 @@ __all__ = ["DG_F32", "DG_BF16", "DG_E4M3", "HeadDesc", "CanvasState", "StopRule"
            "REASON_ENTROPY", "REASON_STABLE", "REASON_CAP", "ST_BAD_TOKEN", "ST_NONFINITE",
            "ST_TIMEOUT", "STOP_OR", "STOP_AND", "KEEP_CONFIDENCE", "KEEP_ENTROPY",
            "REDRAW_UNIFORM", "REDRAW_MASK", "pass_rule", "dg_block_generate", "timeline_us",
-           "DG_NVFP4", "nvfp4_scale_bytes", "dg_nvfp4_pack_scales", "dg_quantize_nvfp4"]
+           "DG_NVFP4", "nvfp4_scale_bytes", "dg_nvfp4_pack_scales", "dg_quantize_nvfp4",
+           "dg_profile_next_head", "dg_profile_next_head_clock", "sm_clock_stats"]
 
 DG_F32, DG_BF16, DG_E4M3, DG_NVFP4 = 0, 1, 2, 3
 DG_TL_DENOISE, DG_TL_HEAD, DG_TL_MERGE, DG_TL_KERNELS = 0, 1, 2, 3
@@ -69,7 +70,8 @@ class LoopParams(C.Structure):
                 ("trace_mean_entropy", C.c_void_p), ("trace_canvas", C.c_void_p),
                 ("trace_h", C.c_void_p), ("trace_argmax", C.c_void_p), ("trace_conf", C.c_void_p),
                 ("trace_entropy", C.c_void_p), ("trace_timeline", C.c_void_p),
-                ("temp_start", C.c_float), ("temp_end", C.c_float), ("row_offset", C.c_uint64)]
+                ("temp_start", C.c_float), ("temp_end", C.c_float), ("row_offset", C.c_uint64),
+                ("trace_sm_clock", C.c_void_p)]
 
 
 class SynthParams(C.Structure):
@@ -117,6 +119,8 @@ def lib():
         L.dg_canvas_step_host.restype = C.c_int
         L.dg_profile_next_head.argtypes = [C.c_void_p, C.c_void_p]
         L.dg_profile_next_head.restype = C.c_int
+        L.dg_profile_next_head_clock.argtypes = [C.c_void_p]
+        L.dg_profile_next_head_clock.restype = C.c_int
         for f in ("dg_workspace_bytes", "dg_canvas_stats", "dg_canvas_step", "dg_canvas_loop"):
             getattr(L, f).restype = C.c_int
         _lib = L
@@ -130,6 +134,29 @@ def dg_profile_next_head(start: torch.cuda.Event, stop: torch.cuda.Event) -> Non
             ev.record()
     _check(lib().dg_profile_next_head(C.c_void_p(start.cuda_event), C.c_void_p(stop.cuda_event)),
            "dg_profile_next_head")
+
+
+def dg_profile_next_head_clock(sample: torch.Tensor) -> None:
+    """Have the next head kernel launched by this thread write its SM clock sample into
+    `sample` (device int64 [4]: clock64 and global-timer ns at begin, then at end)."""
+    if sample.numel() < 4 or sample.element_size() != 8:
+        raise ValueError("the clock sample needs 4 x 8 bytes")
+    _check(lib().dg_profile_next_head_clock(_ptr(sample)), "dg_profile_next_head_clock")
+
+
+def sm_clock_stats(samples) -> dict:
+    """Effective SM clock (MHz) and head duration in SM cycles from clock samples [n, 4]
+    (rows with no sample are skipped)."""
+    t = samples.detach().cpu().view(-1, 4).numpy().view("uint64").astype("float64")
+    ok = (t[:, 3] > t[:, 1]) & (t[:, 2] > t[:, 0])
+    t = t[ok]
+    if not len(t):
+        return {"sm_mhz_effective": None, "head_kcycles": None, "samples": 0}
+    mhz = (t[:, 2] - t[:, 0]) / (t[:, 3] - t[:, 1]) * 1e3
+    import statistics
+    return {"sm_mhz_effective": round(statistics.median(mhz.tolist()), 1),
+            "head_kcycles": round(statistics.median(((t[:, 2] - t[:, 0]) / 1e3).tolist()), 2),
+            "samples": int(len(t))}
 
 
 def dg_status_string(code: int) -> str:
@@ -369,7 +396,8 @@ def prepare_loop(w, canvas, *, B: int, S: int, theta: float, y=None, denoise=Non
                    seed: int = 0, max_passes: int = 48, stable_passes: int = 2,
                    stop_mode: int = STOP_OR, start_pass: int = 0, init_random: bool = True,
                    state=None, n_content: int = 50, s_content: float = 8.0, s_pad: float = 16.0,
-                   trace: bool = False, timeline: bool = False, workspace=None, status=None,
+                   trace: bool = False, timeline: bool = False, sm_clock: bool = False,
+                   workspace=None, status=None,
                    outputs: dict | None = None, keep_rule: int = KEEP_CONFIDENCE,
                    mask_id: int | None = None, temp_start: float = 0.0, temp_end: float = 0.0,
                    row_offset: int = 0) -> "PreparedLoop":
@@ -384,6 +412,8 @@ def prepare_loop(w, canvas, *, B: int, S: int, theta: float, y=None, denoise=Non
     repeated call reuses the captured graph. With timeline=True the result holds
     "trace_timeline" [max_passes, 3, 2] (uint64 stored as int64): per pass, the device global
     timer (ns) at the begin/end of the denoiser (built-in only), the head and the merge kernel.
+    With sm_clock=True it holds "trace_sm_clock" [max_passes, 4]: each pass's head clock sample
+    (sm_clock_stats turns it into the effective SM clock and the head's cycle count).
     """
     dev = w.device
     R = B * S
@@ -426,6 +456,9 @@ def prepare_loop(w, canvas, *, B: int, S: int, theta: float, y=None, denoise=Non
     if timeline:
         out["trace_timeline"] = torch.empty(max_passes, DG_TL_KERNELS, 2, dtype=torch.int64, device=dev)
         params.trace_timeline = _ptr(out["trace_timeline"]).value
+    if sm_clock:
+        out["trace_sm_clock"] = torch.zeros(max_passes, 4, dtype=torch.int64, device=dev)
+        params.trace_sm_clock = _ptr(out["trace_sm_clock"]).value
     L = lib()
     keep = []
     if denoise is None:

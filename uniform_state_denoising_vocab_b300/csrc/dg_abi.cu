@@ -225,6 +225,8 @@ struct Prepared {
     const int32_t* stop = nullptr;           // loop stop flag (device) or null
     float temp_start = 0.f, temp_end = 0.f;  // loop temperature schedule
     int temp_passes = 0;                     // its max_passes, 0 = none
+    unsigned long long* clk = nullptr;       // head SM clock sample (HeadArgs::clk) or null
+    int clk_per_pass = 0;
 };
 
 int prepare(const dg_head_desc* d, void* ws, size_t ws_bytes, Prepared* P, bool need_h = true) {
@@ -241,6 +243,7 @@ int prepare(const dg_head_desc* d, void* ws, size_t ws_bytes, Prepared* P, bool 
 }
 
 thread_local cudaEvent_t t_prof_start = nullptr, t_prof_stop = nullptr;
+thread_local unsigned long long* t_prof_clock = nullptr;
 
 cudaError_t launch_head_only(const dg_head_desc* d, const Prepared& P, uint8_t* ws, uint32_t* status,
                              cudaStream_t stream);
@@ -265,22 +268,28 @@ cudaError_t launch_quantiser(const dg_head_desc* d, const Prepared& P, uint8_t* 
 cudaError_t enqueue_head(const dg_head_desc* d, const Prepared& P, uint8_t* ws, uint32_t* status,
                          cudaStream_t stream) {
     cudaEvent_t e0 = nullptr, e1 = nullptr;
-    if (t_prof_start && t_prof_stop) {
+    Prepared Pc = P;
+    if ((t_prof_start && t_prof_stop) || t_prof_clock) {
         cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
         if (cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone) {
             e0 = t_prof_start;
             e1 = t_prof_stop;
             t_prof_start = t_prof_stop = nullptr;
+            if (t_prof_clock) {
+                Pc.clk = t_prof_clock;
+                Pc.clk_per_pass = 0;
+                t_prof_clock = nullptr;
+            }
         }
     }
-    if (!e0) return launch_head_only(d, P, ws, status, stream);
+    if (!e0) return launch_head_only(d, Pc, ws, status, stream);
     // a0 runs before the bracket so that the events time the head kernel alone
     if (quant_path(P.path)) {
         cudaError_t e = launch_quantiser(d, P, ws, status, stream);
         if (e != cudaSuccess) return e;
     }
     cudaEventRecord(e0, stream);
-    Prepared Q = P;
+    Prepared Q = Pc;
     if (quant_path(Q.path)) Q.path = -Q.path;  // quantisation already done
     cudaError_t e = launch_head_only(d, Q, ws, status, stream);
     cudaEventRecord(e1, stream);
@@ -308,6 +317,8 @@ cudaError_t launch_head_only(const dg_head_desc* d, const Prepared& P, uint8_t* 
     a.temp_passes = P.temp_passes;
     a.w_scale = d->w_scale;
     a.h_scale = d->h_scale;
+    a.clk = P.clk;
+    a.clk_per_pass = P.clk_per_pass;
     cudaError_t e = cudaSuccess;
     switch (P.path) {
     case PATH_SIMT:
@@ -408,6 +419,12 @@ int dg_profile_next_head(void* start_event, void* stop_event) {
     if ((start_event == nullptr) != (stop_event == nullptr)) return DG_ERR_INVALID_ARG;
     t_prof_start = static_cast<cudaEvent_t>(start_event);
     t_prof_stop = static_cast<cudaEvent_t>(stop_event);
+    return DG_OK;
+}
+
+int dg_profile_next_head_clock(unsigned long long* clock_sample) {
+    if (clock_sample && (reinterpret_cast<uintptr_t>(clock_sample) & 7u)) return DG_ERR_ALIGNMENT;
+    t_prof_clock = clock_sample;
     return DG_OK;
 }
 
@@ -591,6 +608,7 @@ void copy_params(dg_loop_params* dst, const dg_loop_params& s) {
     dst->trace_conf = s.trace_conf;
     dst->trace_entropy = s.trace_entropy;
     dst->trace_timeline = s.trace_timeline;
+    dst->trace_sm_clock = s.trace_sm_clock;
 }
 
 void copy_synth(dg_synth_params* dst, const dg_synth_params& s) {
@@ -657,6 +675,8 @@ int build_loop_graph(LoopEntry* E, const Prepared& P) {
     const int passes_per_iter = builtin ? 2 : 1;
     Prepared Ph = P;
     Ph.timeline = k.params.trace_timeline;
+    Ph.clk = k.params.trace_sm_clock;
+    Ph.clk_per_pass = 1;
     Ph.pass_ptr = &ctl->pass;
     Ph.stop = &ctl->stop;
     if (k.params.temp_start > 0.f) {

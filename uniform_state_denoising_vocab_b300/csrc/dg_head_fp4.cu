@@ -125,6 +125,8 @@ __global__ void __launch_bounds__(kFp4Threads, 1)
     const int tl_pass = args.timeline != nullptr ? *args.pass_ptr : 0;
     const float crow_base = pass_crow_base(args);
     if (units > 0) timeline_begin(args.timeline, tl_pass, DG_TL_HEAD);
+    unsigned long long* const clk_slot = units > 0 ? head_clock_slot(args) : nullptr;
+    head_clock_stamp(clk_slot, 0);
     grid_launch_dependents();
 
     if (warp == 0) {
@@ -280,6 +282,7 @@ __global__ void __launch_bounds__(kFp4Threads, 1)
         tmem_dealloc(tmem_base, TMEM_COLS);
     }
     if (units > 0) timeline_end(args.timeline, tl_pass, DG_TL_HEAD);
+    head_clock_stamp(clk_slot, 1);
 }
 
 }  // namespace

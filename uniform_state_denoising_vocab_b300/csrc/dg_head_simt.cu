@@ -32,6 +32,8 @@ __global__ void __launch_bounds__(THREADS)
     const int tl_pass = args.timeline != nullptr ? *args.pass_ptr : 0;
     const float crow_base = pass_crow_base(args);
     if (units > 0) timeline_begin(args.timeline, tl_pass, DG_TL_HEAD);
+    unsigned long long* const clk_slot = units > 0 ? head_clock_slot(args) : nullptr;
+    head_clock_stamp(clk_slot, 0);
     grid_launch_dependents();
     for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
         const int mb = unit % args.MB, grp = unit / args.MB;
@@ -84,6 +86,7 @@ __global__ void __launch_bounds__(THREADS)
                 pack(row_state_partial(st));
     }
     if (units > 0) timeline_end(args.timeline, tl_pass, DG_TL_HEAD);
+    head_clock_stamp(clk_slot, 1);
 }
 
 }  // namespace

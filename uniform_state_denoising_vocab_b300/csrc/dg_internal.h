@@ -63,6 +63,8 @@ struct HeadArgs {
     const int32_t* stop;           // loop mode: non-zero = the loop has ended, do nothing
     float temp_start, temp_end;    // loop temperature schedule (temp_passes > 0)
     int temp_passes;               // max_passes of the schedule, 0 = none
+    unsigned long long* clk;       // SM clock sample [n][4] or null (head_clock_slot)
+    int clk_per_pass;              // 1: row *pass_ptr of clk (loop trace), 0: row 0
 };
 
 // The logit scale of a pass, in base-2 units: crow_base (= inv_temp * log2 e), divided by the
@@ -102,6 +104,21 @@ __device__ __forceinline__ void timeline_begin(unsigned long long* tl, int pass,
 __device__ __forceinline__ void timeline_end(unsigned long long* tl, int pass, int kernel) {
     if (tl != nullptr && threadIdx.x == 0)
         atomicMax(tl + 2 * (static_cast<size_t>(pass) * DG_TL_KERNELS + kernel) + 1, globaltimer_now());
+}
+
+// SM clock sample of a head launch: CTA 0 / thread 0 stores its clock64 and the global timer
+// (ns) when it gets past its dependency wait (slot[0], slot[1]) and when it leaves (slot[2],
+// slot[3]); cycles over nanoseconds is the SM clock the kernel actually ran at, and the cycle
+// count is the kernel's duration independent of that clock.
+__device__ __forceinline__ unsigned long long* head_clock_slot(const HeadArgs& a) {
+    if (a.clk == nullptr || blockIdx.x != 0 || threadIdx.x != 0) return nullptr;
+    return a.clk + 4 * static_cast<size_t>(a.clk_per_pass && a.pass_ptr ? *a.pass_ptr : 0);
+}
+__device__ __forceinline__ void head_clock_stamp(unsigned long long* slot, int i) {
+    if (slot != nullptr) {
+        slot[2 * i] = static_cast<unsigned long long>(clock64());
+        slot[2 * i + 1] = globaltimer_now();
+    }
 }
 
 inline void set_pdl_attr(cudaLaunchAttribute* a) {
