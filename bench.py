@@ -221,9 +221,9 @@ HEAD_SOURCES = {
     "fp4": ["dg_head_fp4.cu", "dg_head_epi.cuh", "dg_common.cuh", "dg_ptx.cuh", "dg_internal.h"],
 }
 TRAFFIC = {
-    "pass_bf16_v262144_d2816": {"bytes": 1.477922e9 + 3.227648e6, "src": "5806b221557a181a"},
-    "loop_e4m3_v262144_d2816": {"bytes": 740.031488e6 + 2.866432e6, "src": "5806b221557a181a"},
-    "pass_nvfp4_v262144_d2816": {"bytes": 417.411584e6 + 3.492864e6, "src": "8b34dc2a8d024d3f"},
+    "pass_bf16_v262144_d2816": {"bytes": 1.477884e9 + 2.997760e6, "src": "ce43c3091c768cb4"},
+    "loop_e4m3_v262144_d2816": {"bytes": 740.012544e6 + 2.898176e6, "src": "ce43c3091c768cb4"},
+    "pass_nvfp4_v262144_d2816": {"bytes": 417.261824e6 + 3.855872e6, "src": "bcdb3555c4914fd7"},
 }
 
 
@@ -243,11 +243,14 @@ ALU_FP32_FLOP_PER_CLK = 148 * 128 * 2   # fp32 FMA lanes x 2 flops, for the CUDA
 
 def tensor_regime(timed_s: float, clocks: dict) -> str:
     """Which measured tensor peak applies to a kernel timed inside a region of `timed_s`
-    seconds: the burst rate for short regions or when the sampled SM clock stayed near its
-    maximum, the sustained (power-capped) rate for seconds-long runs at a lowered clock."""
+    seconds: the sustained (power-capped) rate when the clocks sampled during the region show
+    the power cap holding the SM clock well below its maximum, or, with no clock samples, for a
+    region of a second or more; the burst rate otherwise (short regions, unthrottled clocks)."""
     sm, mx = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
-    near_max = sm is not None and mx and sm >= NEAR_MAX_CLOCK * mx
-    return "burst" if (timed_s < SUSTAINED_MIN_S or near_max) else "sustained"
+    if sm is None or not mx:
+        return "sustained" if timed_s >= SUSTAINED_MIN_S else "burst"
+    capped = "sw_power_cap" in clocks.get("reasons", []) and sm < NEAR_MAX_CLOCK * mx
+    return "sustained" if capped else "burst"
 
 
 def roofline(cfg, r, peaks, peak_kind, step_s, regime="burst"):

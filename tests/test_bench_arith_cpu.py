@@ -39,7 +39,7 @@ def test_roofline_short_region_uses_the_burst_peak_and_is_hbm_bound():
     fraction is achieved GB/s over the copy bandwidth."""
     cfg = CONFIGS["pass_bf16_v262144_d2816"]
     flops, byts = bench.algorithmic(cfg)
-    clocks = {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0}
+    clocks = {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0, "reasons": []}
     regime = bench.tensor_regime(0.0054, clocks)
     assert regime == "burst"
     head_us = 263.3
@@ -57,14 +57,16 @@ def test_roofline_short_region_uses_the_burst_peak_and_is_hbm_bound():
 
 
 def test_tensor_regime_rule():
-    # seconds-long run at a power-capped clock: the sustained rate
-    assert bench.tensor_regime(2.0, {"sm_mhz": 1160.0, "sm_max_mhz": 2032.0}) == "sustained"
-    # seconds-long run that kept the clock near its maximum: burst
-    assert bench.tensor_regime(2.0, {"sm_mhz": 2000.0, "sm_max_mhz": 2032.0}) == "burst"
-    # short region, whatever the clock: burst
-    assert bench.tensor_regime(0.3, {"sm_mhz": 1160.0, "sm_max_mhz": 2032.0}) == "burst"
+    cap = ["sw_power_cap"]
+    # the power cap holding the clock well below its maximum: the sustained rate, however long
+    assert bench.tensor_regime(0.69, {"sm_mhz": 1140.0, "sm_max_mhz": 2032.0, "reasons": cap}) == "sustained"
+    assert bench.tensor_regime(2.0, {"sm_mhz": 1160.0, "sm_max_mhz": 2032.0, "reasons": cap}) == "sustained"
+    # the clock at its maximum (power cap flagged or not): burst
+    assert bench.tensor_regime(2.0, {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0, "reasons": cap}) == "burst"
+    assert bench.tensor_regime(0.005, {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0, "reasons": []}) == "burst"
     # no clock samples: decided by the region's length
     assert bench.tensor_regime(2.0, {"sm_mhz": None, "sm_max_mhz": None}) == "sustained"
+    assert bench.tensor_regime(0.3, {"sm_mhz": None, "sm_max_mhz": None}) == "burst"
 
 
 def test_roofline_sustained_regime_compute_bound_bf16():
