@@ -101,3 +101,25 @@ def test_host_step_in_place_canvas(dg):
     ref = dg.dg_canvas_step(hd["h"], w, torch.from_numpy(c0).cuda(), 32, 4, 0, B=B, S=S)
     torch.cuda.synchronize()
     assert torch.equal(c, ref["canvas"].cpu())
+
+
+def test_host_step_pageable_outputs(dg):
+    """Outputs in pageable host memory and in page-locked host memory both receive the device
+    step's results (the read-back copies are synchronous for the former)."""
+    B, S, V, d = 2, 256, 3000, 256
+    hd, w, _ = _case(dg, "bf16", B, S, V, d, 7)
+    h = hd["h"].cpu().pin_memory()
+    c0 = torch.from_numpy(np.random.default_rng(2).integers(0, V, B * S).astype(np.int32))
+    out_pageable, mean_pageable = torch.empty(B * S, dtype=torch.int32), torch.empty(B)
+    out_pinned = torch.empty(B * S, dtype=torch.int32).pin_memory()
+    mean_pinned = torch.empty(B).pin_memory()
+    dg.dg_canvas_step_host(h, w, c0.pin_memory(), 32, 4, 1, B=B, S=S, canvas_out=out_pageable,
+                           mean_entropy=mean_pageable)
+    dg.dg_canvas_step_host(h, w, c0.pin_memory(), 32, 4, 1, B=B, S=S, canvas_out=out_pinned,
+                           mean_entropy=mean_pinned)
+    torch.cuda.synchronize()
+    ref = dg.dg_canvas_step(hd["h"], w, c0.cuda(), 32, 4, 1, B=B, S=S)
+    torch.cuda.synchronize()
+    for out, mean in ((out_pageable, mean_pageable), (out_pinned, mean_pinned)):
+        assert torch.equal(out, ref["canvas"].cpu())
+        assert torch.equal(mean, ref["mean_entropy"].cpu())
