@@ -11,8 +11,9 @@
 // Why a pair: one tcgen05.mma.cta_group::2 computes a 256 x 256 tile over two SMs. Each CTA
 // stages 128 slot rows of h and 128 of the tile's 256 vocabulary rows of W, so every W byte
 // crosses L2 -> SM once per pair (twice with two independent 128-row CTAs), and each SM's
-// tensor core reads half as many B bytes from shared memory per FLOP. Stages are 32 KB per CTA,
-// so six fit in shared memory and cover DRAM latency under load.
+// tensor core reads half as many B bytes from shared memory per FLOP. Stages are 32 KB per CTA:
+// seven fit in shared memory for bf16 (six for E4M3, which also stages the tile's column scales),
+// and the loads in flight cover DRAM latency under load.
 //
 // Roles (192 threads per CTA; cluster of 2, CTA rank 0 = "leader"):
 //   warp 0     producer: one thread waits for a free stage (its own `empty` barrier, signalled
@@ -39,17 +40,21 @@ namespace {
 
 constexpr int BM = 128;               // slot rows per CTA (256 per pair)
 constexpr int BN = kTcBN;             // vocabulary ids per tile (256; 128 staged per CTA)
-constexpr int STAGES = kTc2Stages;
+// Ring depth: the bf16 head stages no column scales, which leaves room for one more stage.
+template <int KIND>
+constexpr int stages_of() { return KIND == 0 ? kTc2Stages + 1 : kTc2Stages; }
+constexpr int kMaxStages = kTc2Stages + 1;
 constexpr int A_BYTES = BM * 128;     // one 128-byte K slice of 128 rows
 constexpr int B_BYTES = (BN / 2) * 128;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 4 * BN * 4 + 256;
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+template <int KIND>
+constexpr int smem_of() { return 1024 + stages_of<KIND>() * STAGE_BYTES + (KIND == 1 ? 4 * BN * 4 : 0) + 256; }
+static_assert(smem_of<0>() <= 227 * 1024 && smem_of<1>() <= 227 * 1024, "shared memory budget");
 
 struct SmemCtl {
-    uint64_t full[STAGES];   // leader: both CTAs' A/B halves of a stage have landed
-    uint64_t empty[STAGES];  // each CTA: the stage's MMAs are done (commit multicast)
+    uint64_t full[kMaxStages];   // leader: both CTAs' A/B halves of a stage have landed
+    uint64_t empty[kMaxStages];  // each CTA: the stage's MMAs are done (commit multicast)
     uint64_t tfull[2];       // each CTA: accumulator complete (commit multicast)
     uint64_t tempty[2];      // leader: accumulator drained by both CTAs (8 warp arrivals)
     uint64_t drain;          // leader: every MMA issued has completed
@@ -71,9 +76,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
+    constexpr int STAGES = stages_of<KIND>();
     uint8_t* sB = smem + STAGES * A_BYTES;
     float* s_csc = reinterpret_cast<float*>(sB + STAGES * B_BYTES);  // [4 epilogue warps][BN]
-    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(s_csc + 4 * BN);
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(s_csc + (KIND == 1 ? 4 * BN : 0));
     const volatile int* abort_flag = &ctl->abort;
 
     const int warp = threadIdx.x >> 5;
@@ -259,12 +265,13 @@ cudaError_t launch_head_tc2(int kind, const CUtensorMap& ma, const CUtensorMap& 
                             const HeadArgs& args, int n_pairs, cudaStream_t stream) {
     const void* fn = kind == 0 ? reinterpret_cast<const void*>(head_tc2_kernel<0>)
                                : reinterpret_cast<const void*>(head_tc2_kernel<1>);
-    cudaError_t e = ensure_smem_attr(fn, SMEM_BYTES);
+    const int smem = kind == 0 ? smem_of<0>() : smem_of<1>();
+    cudaError_t e = ensure_smem_attr(fn, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * n_pairs);
     cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -286,13 +293,13 @@ int head_tc2_max_pairs() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
     if (cached[dev] > 0) return cached[dev];
-    if (ensure_smem_attr(reinterpret_cast<const void*>(head_tc2_kernel<0>), SMEM_BYTES) !=
+    if (ensure_smem_attr(reinterpret_cast<const void*>(head_tc2_kernel<0>), smem_of<0>()) !=
         cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2);
     cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.dynamicSmemBytes = smem_of<0>();
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;

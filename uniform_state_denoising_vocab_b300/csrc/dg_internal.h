@@ -17,7 +17,7 @@ namespace dg {
 constexpr int kTcBM = 128;
 constexpr int kTcBN = 256;
 constexpr int kTcStages = 4;
-constexpr int kTc2Stages = 6;    // pair kernel: 32 KB stages (128 h rows + 128 W rows)
+constexpr int kTc2Stages = 6;    // pair kernel: 32 KB stages (128 h rows + 128 W rows); bf16 +1
 constexpr int kTcThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 // NVFP4 head: vocabulary rows per tile, accumulator buffers, pipeline stages and threads. TMEM
 // holds kFp4Acc accumulators of kFp4BN columns plus the scale factors of every stage in flight; of
