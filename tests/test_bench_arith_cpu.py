@@ -58,15 +58,26 @@ def test_roofline_short_region_uses_the_burst_peak_and_is_hbm_bound():
 
 def test_tensor_regime_rule():
     cap = ["sw_power_cap"]
-    # the power cap holding the clock well below its maximum: the sustained rate, however long
-    assert bench.tensor_regime(0.69, {"sm_mhz": 1140.0, "sm_max_mhz": 2032.0, "reasons": cap}) == "sustained"
+    # a seconds-long region with the power cap holding the clock down: the sustained rate
     assert bench.tensor_regime(2.0, {"sm_mhz": 1160.0, "sm_max_mhz": 2032.0, "reasons": cap}) == "sustained"
+    # shorter than a second: burst, whatever the clock
+    assert bench.tensor_regime(0.69, {"sm_mhz": 1140.0, "sm_max_mhz": 2032.0, "reasons": cap}) == "burst"
+    assert bench.tensor_regime(0.005, {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0, "reasons": []}) == "burst"
     # the clock at its maximum (power cap flagged or not): burst
     assert bench.tensor_regime(2.0, {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0, "reasons": cap}) == "burst"
-    assert bench.tensor_regime(0.005, {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0, "reasons": []}) == "burst"
     # no clock samples: decided by the region's length
     assert bench.tensor_regime(2.0, {"sm_mhz": None, "sm_max_mhz": None}) == "sustained"
     assert bench.tensor_regime(0.3, {"sm_mhz": None, "sm_max_mhz": None}) == "burst"
+
+
+def test_roofline_never_uses_a_sustained_peak_the_kernel_beats():
+    """8 canvases at 2,109 us: 1,434 TFLOP/s, above the 1,350 sustained figure -> the burst peak."""
+    cfg = CONFIGS["pass_bf16_b8_v262144_d2816"]
+    flops, byts = bench.algorithmic(cfg)
+    r = {"head_ms": [2.1093], "flops": flops, "bytes": byts}
+    out = bench.roofline(cfg, r, PEAKS, "measured", step_s=2.11e-3, regime="sustained")
+    assert out["regime"] == "burst" and out["bound"] == "tensor" and out["peak"] == 1700.0
+    assert out["frac"] == pytest.approx(flops / 2.1093e-3 / 1e12 / 1700.0) and out["frac"] < 1.0
 
 
 def test_roofline_sustained_regime_compute_bound_bf16():
