@@ -93,6 +93,7 @@ def _nvfp4_case(dg, B, S, V, d, seed):
     (2, 100, 3001, 512),     # rows not a multiple of 128; canvases straddle row blocks
     (1, 64, 777, 768),       # short canvas
     (1, 256, 2083, 2816),    # full hidden size
+    (3, 100, 1000, 256),     # 300 rows: three row blocks, the last holding 44 rows
 ])
 def test_nvfp4_pass_parity(dg, orc, B, S, V, d):
     hb, (wq, wbs, wsc), tw, twb, tws, canvas = _nvfp4_case(dg, B, S, V, d, V + d)
