@@ -83,6 +83,8 @@ def test_fp32_pass_v4096_d64(dg, orc):
     (1, 256, 256, 64),       # exactly one tile
     (1, 256, 16, 64),        # vocabulary smaller than one 32-column chunk
     (1, 256, 2083, 2816),    # full hidden size, ragged vocabulary
+    (1, 256, 1000, 72),      # K tail: the second 64-element slice holds 8 elements (TMA zero fill)
+    (2, 150, 2000, 200),     # K tail on the pair kernel (300 rows, two 256-row blocks)
 ])
 def test_bf16_shapes(dg, orc, B, S, V, d):
     g, o, _ = _run_step(dg, orc, B, S, V, d, "bf16", K=min(32, S), seed=V + d, pass_=3)
@@ -99,7 +101,8 @@ def test_fp32_shapes(dg, orc, B, S, V, d):
     check_select(g, o, B, S, V, 20, 5, 1, orc.draw)
 
 
-@pytest.mark.parametrize("B,S,V,d", [(1, 256, 1000, 256), (2, 200, 2500, 2816)])
+@pytest.mark.parametrize("B,S,V,d", [(1, 256, 1000, 256), (2, 200, 2500, 2816),
+                                     (1, 256, 1000, 208), (1, 100, 700, 48)])  # K tails
 def test_e4m3_quantised_head(dg, orc, B, S, V, d):
     g, o, _ = _run_step(dg, orc, B, S, V, d, "e4m3", K=32, seed=11, pass_=0)
     check_stats(g, o, TOL["e4m3"])
