@@ -125,6 +125,17 @@ def test_e4m3_prequantised_h_matches_device_quantiser(dg, orc):
         assert torch.equal(a[k], b[k]), k
 
 
+@pytest.mark.parametrize("B,S,K", [(3, 1, 0), (3, 1, 1), (1, 1024, 500), (2, 513, 100)])
+def test_canvas_size_extremes(dg, orc, B, S, K):
+    """One-slot canvases (each a cluster with seven idle CTAs), the largest canvas the merge
+    supports (1024 slots, 128 per CTA of its cluster) and a ragged one."""
+    g, o, _ = _run_step(dg, orc, B, S, 3000, 128, "bf16", K=K, seed=S + K, pass_=5)
+    check_stats(g, o, TOL["bf16"])
+    check_select(g, o, B, S, 3000, K, S + K, 5, orc.draw)
+    assert int(g["status"][0]) == 0
+    assert np.allclose(g["mean_entropy"], o["mean_entropy"], atol=TOL["bf16"])
+
+
 @pytest.mark.parametrize("K", [0, 1, 255, 256, 1000])
 def test_keep_edges(dg, orc, K):
     g, o, canvas = _run_step(dg, orc, 2, 256, 3000, 128, "bf16", K=K, seed=7, pass_=9)
