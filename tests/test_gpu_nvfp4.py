@@ -94,6 +94,7 @@ def _nvfp4_case(dg, B, S, V, d, seed):
     (1, 64, 777, 768),       # short canvas
     (1, 256, 2083, 2816),    # full hidden size
     (3, 100, 1000, 256),     # 300 rows: three row blocks, the last holding 44 rows
+    (1, 256, 600, 3328),     # 13 K slices, past the full hidden size
 ])
 def test_nvfp4_pass_parity(dg, orc, B, S, V, d):
     hb, (wq, wbs, wsc), tw, twb, tws, canvas = _nvfp4_case(dg, B, S, V, d, V + d)
