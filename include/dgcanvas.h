@@ -377,6 +377,16 @@ DG_API int dg_profile_next_head(void* start_event, void* stop_event);
  */
 DG_API int dg_profile_next_head_clock(unsigned long long* clock_sample);
 
+/*
+ * Self-test of the failure detection every kernel relies on: launches one kernel on `stream`
+ * whose single mbarrier wait can never complete (nothing arrives on it). The wait gives up after
+ * its wall-time bound (about 2 s, the bound of every on-device wait in this library), the kernel
+ * sets DG_ST_TIMEOUT in *status (device, caller-owned, sticky bits OR-ed in) and returns, and the
+ * CUDA context stays usable: no trap, no fault. Returns DG_ERR_INVALID_ARG for a NULL status,
+ * DG_ERR_UNSUPPORTED off sm_103, DG_ERR_CUDA if the launch fails.
+ */
+DG_API int dg_selftest_wait_timeout(uint32_t* status, dg_stream_t stream);
+
 /* Human-readable name of a DG_ERR_* code or DG_ST_* bit set. */
 DG_API const char* dg_status_string(int code);
 

@@ -134,6 +134,10 @@ def test_host_step_argument_checks(dg):
                                  None, None) == -1
 
 
+def test_selftest_rejects_null_status(dg):
+    assert dg.lib().dg_selftest_wait_timeout(None, None) == -1
+
+
 def test_status_strings(dg):
     for code in (0, -1, -2, -3, -4, -5, 1, 2, 4):
         s = dg.dg_status_string(code)

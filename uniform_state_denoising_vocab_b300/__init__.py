@@ -24,7 +24,8 @@ __all__ = ["DG_F32", "DG_BF16", "DG_E4M3", "HeadDesc", "CanvasState", "StopRule"
            "ST_TIMEOUT", "STOP_OR", "STOP_AND", "KEEP_CONFIDENCE", "KEEP_ENTROPY",
            "REDRAW_UNIFORM", "REDRAW_MASK", "pass_rule", "dg_block_generate", "timeline_us",
            "DG_NVFP4", "nvfp4_scale_bytes", "dg_nvfp4_pack_scales", "dg_quantize_nvfp4",
-           "dg_profile_next_head", "dg_profile_next_head_clock", "sm_clock_stats"]
+           "dg_profile_next_head", "dg_profile_next_head_clock", "sm_clock_stats",
+           "dg_selftest_wait_timeout"]
 
 DG_F32, DG_BF16, DG_E4M3, DG_NVFP4 = 0, 1, 2, 3
 DG_TL_DENOISE, DG_TL_HEAD, DG_TL_MERGE, DG_TL_KERNELS = 0, 1, 2, 3
@@ -121,6 +122,8 @@ def lib():
         L.dg_profile_next_head.restype = C.c_int
         L.dg_profile_next_head_clock.argtypes = [C.c_void_p]
         L.dg_profile_next_head_clock.restype = C.c_int
+        L.dg_selftest_wait_timeout.argtypes = [C.c_void_p, C.c_void_p]
+        L.dg_selftest_wait_timeout.restype = C.c_int
         for f in ("dg_workspace_bytes", "dg_canvas_stats", "dg_canvas_step", "dg_canvas_loop"):
             getattr(L, f).restype = C.c_int
         _lib = L
@@ -157,6 +160,15 @@ def sm_clock_stats(samples) -> dict:
     return {"sm_mhz_effective": round(statistics.median(mhz.tolist()), 1),
             "head_kcycles": round(statistics.median(((t[:, 2] - t[:, 0]) / 1e3).tolist()), 2),
             "samples": int(len(t))}
+
+
+def dg_selftest_wait_timeout(status=None, stream=None) -> torch.Tensor:
+    """Launch the library's self-test of its bounded waits: one kernel whose only wait can never
+    complete gives up after the wall-time bound (about 2 s) and sets ST_TIMEOUT in the returned
+    status word (enqueued on `stream`; synchronise before reading it)."""
+    st = torch.zeros(1, dtype=torch.int32, device="cuda") if status is None else status
+    _check(lib().dg_selftest_wait_timeout(_ptr(st), _stream(stream)), "dg_selftest_wait_timeout")
+    return st
 
 
 def dg_status_string(code: int) -> str:

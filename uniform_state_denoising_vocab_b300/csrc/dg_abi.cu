@@ -415,6 +415,17 @@ extern "C" {
 
 int dg_version(void) { return 101; }
 
+int dg_selftest_wait_timeout(uint32_t* status, dg_stream_t stream) {
+    dg::NvtxRange nvtx_range("dg_selftest_wait_timeout");
+    if (!status) return DG_ERR_INVALID_ARG;
+    DeviceInfo di;
+    const int rc = device_info(&di);
+    if (rc != DG_OK) return rc;
+    return launch_wait_selftest(status, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? DG_OK
+               : DG_ERR_CUDA;
+}
+
 int dg_profile_next_head(void* start_event, void* stop_event) {
     if ((start_event == nullptr) != (stop_event == nullptr)) return DG_ERR_INVALID_ARG;
     t_prof_start = static_cast<cudaEvent_t>(start_event);

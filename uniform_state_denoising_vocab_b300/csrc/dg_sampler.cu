@@ -721,6 +721,21 @@ cudaError_t launch_quant_rows(const uint16_t* h, int R, int d, uint8_t* q, float
                               q, scale, status);
 }
 
+// Self-test of the bounded waits: one thread waits on an mbarrier that nothing ever arrives on,
+// with the same wait the head kernels use. It gives up after the wall-time bound (kWaitNs), sets
+// DG_ST_TIMEOUT and returns, as a head kernel does when a wait of one of its roles runs out.
+__global__ void wait_selftest_kernel(uint32_t* status) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    if (!mbar_wait(&bar, 0)) flag_status(status, DG_ST_TIMEOUT);
+}
+
+cudaError_t launch_wait_selftest(uint32_t* status, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(status);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_loop_init(int32_t* canvas, int R, int S, int B, int V, uint64_t seed,
                              int init_random, int mask_id, uint64_t row_offset,
                              dg_canvas_state* state, int keep_stable, LoopCtl* ctl,
