@@ -409,6 +409,12 @@ void set_stats(SelectArgs* s, const Prepared& P, uint8_t* ws, int32_t* argmax, f
 }  // namespace
 }  // namespace dg
 
+namespace dg {
+// dg_sampler.cu: one kernel whose only wait can never complete; it must end by its wall-time
+// bound with DG_ST_TIMEOUT set in *status.
+cudaError_t launch_wait_selftest(uint32_t* status, cudaStream_t stream);
+}  // namespace dg
+
 using namespace dg;
 
 extern "C" {

@@ -216,10 +216,6 @@ cudaError_t launch_loop_init(int32_t* canvas, int R, int S, int B, int V, uint64
                              int start_pass, int max_passes, uint32_t* status,
                              unsigned long long* timeline, cudaStream_t stream);
 
-// One kernel whose only wait can never complete: it must end by its wall-time bound with
-// DG_ST_TIMEOUT set in *status (dg_selftest_wait_timeout).
-cudaError_t launch_wait_selftest(uint32_t* status, cudaStream_t stream);
-
 // Copy rows of one pass into a trace buffer at offset pass * bytes (pass read on device).
 cudaError_t launch_trace_copy(const void* src, void* dst, size_t bytes, const LoopCtl* ctl,
                               cudaStream_t stream);
