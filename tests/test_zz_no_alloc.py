@@ -37,7 +37,7 @@ def _case(B, S, V, d, seed):
     return h, w, c
 
 
-def _noalloc(dg, h, w, canvas, B, S, K, seed, pass_):
+def _noalloc(dg, h, w, canvas, B, S, K, seed, pass_, **desc_kw):
     R = B * S
     out = {"canvas": torch.empty(R, dtype=torch.int32, device="cuda"),
            "argmax": torch.empty(R, dtype=torch.int32, device="cuda"),
@@ -45,7 +45,7 @@ def _noalloc(dg, h, w, canvas, B, S, K, seed, pass_):
            "kept": torch.empty(R, dtype=torch.uint8, device="cuda"),
            "mean_entropy": torch.empty(B, device="cuda"),
            "status": torch.zeros(1, dtype=torch.int32, device="cuda")}
-    desc = dg.make_desc(h, w, B=B, S=S)
+    desc = dg.make_desc(h, w, B=B, S=S, **desc_kw)
     p = lambda t: C.c_void_p(t.data_ptr())
     rc = dg.lib().dg_canvas_step_noalloc(
         C.byref(desc), p(canvas), p(out["canvas"]), K, C.c_uint64(seed), C.c_uint32(pass_),
@@ -87,6 +87,37 @@ def test_noalloc_largest_workload_shape_that_fits(dg):
         r = dg.dg_canvas_step(h, w, c, 32, seed, p, B=B, S=S)
         torch.cuda.synchronize()
         assert int(g["status"][0]) == 0
+        for k in ("canvas", "argmax", "kept", "conf", "entropy", "mean_entropy"):
+            assert torch.equal(g[k], r[k]), k
+
+
+@pytest.mark.parametrize("precision", ["e4m3", "nvfp4"])
+def test_noalloc_quantised_heads_match_workspace_step(dg, precision):
+    """bf16 hidden states against an E4M3 or NVFP4 head: the pass quantises h inside the array
+    (quantised rows, row scales and, for NVFP4, the block scales in the head's layout) before the
+    head reads it; two calls in a row, bit-identical to dg_canvas_step."""
+    from workloads import quantize_rows_e4m3_bits, quantize_rows_nvfp4_bits
+    B, S, V, d = 1, 256, 3000, 512
+    rng = np.random.default_rng(21)
+    h = torch.from_numpy(rng.standard_normal((B * S, d)).astype(np.float32)).to(torch.bfloat16).cuda()
+    wf = torch.from_numpy((rng.standard_normal((V, d)) / np.sqrt(d)).astype(np.float32))
+    wbits = wf.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).reshape(-1)
+    c = torch.from_numpy(rng.integers(0, V, B * S).astype(np.int32)).cuda()
+    if precision == "e4m3":
+        wq, wsc = quantize_rows_e4m3_bits(wbits, V, d)
+        w = torch.from_numpy(wq.reshape(V, d)).cuda()
+        kw = {"w_scale": torch.from_numpy(wsc).cuda(), "w_dtype": dg.DG_E4M3}
+    else:
+        wq, wbs, wsc = quantize_rows_nvfp4_bits(wbits, V, d)
+        w = torch.from_numpy(wq.reshape(V, d // 2)).cuda()
+        twb = dg.dg_nvfp4_pack_scales(torch.from_numpy(wbs.reshape(V, d // 16)).cuda(), V, d)
+        kw = {"w_scale": torch.from_numpy(wsc).cuda(), "w_dtype": dg.DG_NVFP4,
+              "w_block_scale": twb}
+    for seed, p in ((4, 0), (5, 1)):
+        g = _noalloc(dg, h, w, c, B, S, 32, seed, p, **kw)
+        r = dg.dg_canvas_step(h, w, c, 32, seed, p, B=B, S=S, **kw)
+        torch.cuda.synchronize()
+        assert int(g["status"][0]) == 0 and int(r["status"][0]) == 0
         for k in ("canvas", "argmax", "kept", "conf", "entropy", "mean_entropy"):
             assert torch.equal(g[k], r[k]), k
 
