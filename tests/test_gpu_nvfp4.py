@@ -50,6 +50,14 @@ def test_device_quantiser_matches_oracle(dg, orc):
     x[:d] = 0                         # an all-zero row
     x[d:d + 16] = 0                   # an all-zero block in a non-zero row
     x[2 * d:3 * d] *= 1e-30           # tiny values (subnormal block scales)
+    # row 3: exact ties. g = 2^-10 (amax 2688 * 2^-10), a block of scale 1.875 (its maximum
+    # 11.25 * 2^-10) whose elements sit on the midpoints between E2M1 magnitudes: the quotient by
+    # the unit lands exactly on them and must round to the even code
+    unit = 1.875 * 2.0**-10
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    x[3 * d:4 * d] = 0
+    x[3 * d] = 2688 * 2.0**-10
+    x[3 * d + 16:3 * d + 32] = [6.0 * unit] + [m * unit for m in mids] + [-m * unit for m in mids] + [0.0]
     hb = _bits(x)
     got = dg.dg_quantize_nvfp4(dev_bf16(hb, (R, d)))
     torch.cuda.synchronize()

@@ -189,3 +189,69 @@ def test_nvfp4_quantiser_error_bound(orc):
     mag = np.abs(x) / np.where(unit > 0, unit, 1)
     step = np.where(mag < 2, 0.5, np.where(mag < 4, 1.0, 2.0))
     assert (np.abs(dec - x) <= step / 2 * unit * (1 + 1e-6) + 1e-300).all()
+
+
+def _e4m3_nearest_even_positive(t, table):
+    """Brute force: the positive finite E4M3 code (0x00..0x7E, values from the OCP-pinned decoder)
+    nearest to t >= 0, ties to the even code; t at or past 448 saturates to 0x7E."""
+    if t >= 448.0:
+        return 0x7E
+    return min(range(0x7F), key=lambda c: (abs(table[c] - t), c & 1))
+
+
+def test_nvfp4_quantiser_brute_force_scales_and_codes(orc):
+    """Every row scale, block scale and code of the NVFP4 quantiser against an independent
+    determination: the row scale g = fp32(amax / 2688); each block's scale the E4M3 value nearest
+    to fp32(bmax / fp32(6 g)) found by searching all 127 finite codes (ties to even, saturating at
+    448; a zero scale zeroes the block); each code the E2M1 value nearest to
+    fp32(h / fp32(value(scale) g)) found by searching the 8 magnitudes (ties to even, saturating
+    at 6). Rows span six decades within a row (so that some block scales are E4M3 subnormals or
+    round to zero) and include an all-zero block."""
+    table = [float(v) for v in orc.e4m3_value(np.arange(0x7F, dtype=np.uint8))]
+    rng = np.random.default_rng(29)
+    R, d = 6, 128
+    h = (rng.standard_normal(R * d) * np.exp(3.0 * rng.standard_normal(R * d))).astype(np.float32)
+    h[16:32] = 0.0                      # row 0, block 1: all zero
+    h[d:d + 16] *= np.float32(1e-6)     # row 1, block 0: tiny next to the row maximum
+    hb = _bf16(h)
+    x = (hb.astype(np.uint32) << 16).view(np.float32).reshape(R, d)
+    q, bs, sc = orc.quant_rows_nvfp4(hb, R, d)
+    codes = np.stack([q & 0xF, q >> 4], axis=1).reshape(R, d)
+    bs = bs.reshape(R, d // 16)
+    f32 = np.float32
+    for r in range(R):
+        amax = f32(np.abs(x[r]).max())
+        g = f32(amax / f32(2688.0))
+        assert sc[r] == g, r
+        for b in range(d // 16):
+            blk = x[r, 16 * b:16 * b + 16]
+            t = f32(f32(np.abs(blk).max()) / f32(f32(6.0) * g))
+            want_s = _e4m3_nearest_even_positive(float(t), table)
+            assert bs[r, b] == want_s, (r, b)
+            unit = f32(f32(table[want_s]) * g)
+            for k in range(16):
+                if want_s == 0:
+                    want_c = 0
+                else:
+                    want_c = _e2m1_nearest_even(f32(blk[k] / unit))
+                assert codes[r, 16 * b + k] == want_c, (r, b, k)
+    # the blocks built to test the corners really reached them
+    assert bs[0, 1] == 0 and not codes[0, 16:32].any()
+    assert bs[1, 0] < 0x08   # an E4M3 subnormal (or zero) block scale
+
+    # Exact ties. amax = 2688 * 2^-10 makes g = 2^-10 exactly; a block whose maximum is
+    # 11.25 * 2^-10 gets the scale 1.875 (E4M3 0x3F) exactly, so its unit is 1.875 * 2^-10, whose
+    # reciprocal is inexact. The block's other elements sit exactly on the midpoints between E2M1
+    # magnitudes (times the unit, all exact in bf16): the division lands on the midpoint and
+    # rounds to the even code, where multiplying by the rounded reciprocal of the unit lands just
+    # above 1.25, 2.5 and 5 and rounds up to the odd code.
+    unit = 1.875 * 2.0**-10
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    blk1 = [6.0 * unit] + [m * unit for m in mids] + [-m * unit for m in mids] + [0.0]
+    row = np.array([2688 * 2.0**-10] + [0.0] * 15 + blk1, np.float32)
+    q, bs, sc = orc.quant_rows_nvfp4(_bf16(row), 1, 32)
+    assert sc[0] == np.float32(2.0**-10) and bs[1] == 0x3F
+    codes = np.stack([q & 0xF, q >> 4], axis=1).reshape(-1)[16:]
+    even = {0.25: 0, 0.75: 2, 1.25: 2, 1.75: 4, 2.5: 4, 3.5: 6, 5.0: 6}
+    want = [7] + [even[m] for m in mids] + [0x8 | even[m] for m in mids] + [0]
+    assert list(codes) == want
