@@ -255,3 +255,40 @@ def test_nvfp4_quantiser_brute_force_scales_and_codes(orc):
     even = {0.25: 0, 0.75: 2, 1.25: 2, 1.75: 4, 2.5: 4, 3.5: 6, 5.0: 6}
     want = [7] + [even[m] for m in mids] + [0x8 | even[m] for m in mids] + [0]
     assert list(codes) == want
+
+
+def test_quant_rows_brute_force_codes(orc):
+    """Every code and scale of the per-row E4M3 quantiser against an independent determination:
+    scale = fp32(amax / 448), inv = fp32(448 / amax), and each code the E4M3 value nearest to
+    fp32(h * inv) found by searching all finite codes (ties to the even code, sign kept,
+    saturating at 448). Rows of wide dynamic range reach the subnormal codes; two built rows put
+    products exactly on E4M3 midpoints (or one fp32 step off them), where dividing by the scale
+    instead of multiplying by inv would land on the other side."""
+    table = [float(v) for v in orc.e4m3_value(np.arange(0x7F, dtype=np.uint8))]
+    rng = np.random.default_rng(31)
+    R, d = 10, 64
+    x = (rng.standard_normal(R * d) * np.exp(2.5 * rng.standard_normal(R * d))).astype(np.float32)
+    x[8 * d:] = 0
+    # amax 1.9375: 0.0113525390625 * fp32(448 / 1.9375) = 2.625 exactly (midpoint of 2.5, 2.75)
+    x[8 * d:8 * d + 3] = [1.9375, 0.0113525390625, 0.022705078125]
+    # amax 3.1875: the product is one step above the midpoint 1.3125 (the quotient lands on it)
+    x[9 * d:9 * d + 3] = [3.1875, 0.00933837890625, 0.0186767578125]
+    hb = _bf16(x)
+    xv = (hb.astype(np.uint32) << 16).view(np.float32).reshape(R, d)
+    q, sc = orc.quant_rows_e4m3(hb, R, d)
+    q = q.reshape(R, d)
+    f32 = np.float32
+    subnormal = 0
+    for r in range(R):
+        amax = f32(np.abs(xv[r]).max())
+        assert sc[r] == f32(amax / f32(448.0)), r
+        inv = f32(f32(448.0) / amax)
+        for k in range(d):
+            t = f32(xv[r, k] * inv)
+            mag = _e4m3_nearest_even_positive(abs(float(t)), table)
+            want = (0x80 if np.signbit(t) else 0) | mag
+            if mag == 0:
+                want = q[r, k] & 0x80   # a zero keeps whichever sign bit the quantiser gave it
+            assert q[r, k] == want, (r, k)
+            subnormal += 0 < mag < 0x08
+    assert subnormal > 0
