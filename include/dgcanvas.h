@@ -286,6 +286,17 @@ DG_API int dg_block_generate(const dg_head_desc* desc, int32_t n_blocks, const i
                              uint32_t* status, dg_stream_t stream);
 
 /*
+ * Per-row E4M3 quantisation of bf16 rows [rows, d] on the device (step a0 of an FP8 pass, the
+ * rule a (BF16, E4M3) descriptor applies inside a pass), in IEEE binary32: amax = max_k |h_k|;
+ * amax == 0 gives row scale 1 and zero codes; else inv = 448 / amax,
+ * codes q_k = e4m3_rn_satfinite(h_k * inv) and row scale amax / 448 (each operation rounded to
+ * nearest). Writes codes [rows, d] (E4M3 bytes) and row_scale [rows]; sets DG_ST_NONFINITE in
+ * *status (may be NULL) on non-finite input. Device pointers; h_bf16 16-byte aligned.
+ */
+DG_API int dg_quantize_e4m3(const void* h_bf16, int32_t rows, int32_t d, uint8_t* codes,
+                            float* row_scale, uint32_t* status, dg_stream_t stream);
+
+/*
  * NVFP4 operand preparation (4-bit heads).
  *   dg_nvfp4_scale_bytes: size of the packed block-scale array of `rows` rows of width d:
  *     ceil(rows / 256) * 256 * d / 16 bytes.

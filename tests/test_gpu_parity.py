@@ -109,6 +109,30 @@ def test_e4m3_quantised_head(dg, orc, B, S, V, d):
     check_select(g, o, B, S, V, 32, 11, 0, orc.draw)
 
 
+@pytest.mark.parametrize("d", [64, 300])
+def test_device_e4m3_quantiser_bit_for_bit(dg, orc, d):
+    """dg_quantize_e4m3 (the device's step a0) against the oracle's quantiser code by code:
+    rows of wide dynamic range (subnormal codes, saturation at 448), an all-zero row, and rows
+    whose products sit exactly on E4M3 midpoints or one fp32 step off them."""
+    rng = np.random.default_rng(d)
+    R = 40
+    x = (rng.standard_normal(R * d) * np.exp(2.5 * rng.standard_normal(R * d))).astype(np.float32)
+    x[:d] = 0
+    x[d:2 * d] = 0
+    x[d:d + 3] = [1.9375, 0.0113525390625, 0.022705078125]
+    x[2 * d:3 * d] = 0
+    x[2 * d:2 * d + 3] = [3.1875, 0.00933837890625, 0.0186767578125]
+    hb = _bits(x)
+    got = dg.dg_quantize_e4m3(dev_bf16(hb, (R, d)))
+    torch.cuda.synchronize()
+    q, sc = orc.quant_rows_e4m3(hb, R, d)
+    assert int(got["status"][0]) == 0
+    assert np.array_equal(host(got["scale"]), sc)
+    gq = host(got["codes"]).reshape(-1)
+    zero = lambda c: np.where((c & 0x7F) == 0, 0, c)   # -0 and +0 are the same value
+    assert np.array_equal(zero(gq), zero(q))
+
+
 def test_e4m3_prequantised_h_matches_device_quantiser(dg, orc):
     """bf16 h quantised on the device must give the same statistics, bit for bit, as the
     oracle-quantised E4M3 h passed in directly (the quantiser is exact in fp32)."""

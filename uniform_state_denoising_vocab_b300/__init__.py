@@ -25,7 +25,7 @@ __all__ = ["DG_F32", "DG_BF16", "DG_E4M3", "HeadDesc", "CanvasState", "StopRule"
            "REDRAW_UNIFORM", "REDRAW_MASK", "pass_rule", "dg_block_generate", "timeline_us",
            "DG_NVFP4", "nvfp4_scale_bytes", "dg_nvfp4_pack_scales", "dg_quantize_nvfp4",
            "dg_profile_next_head", "dg_profile_next_head_clock", "sm_clock_stats",
-           "dg_selftest_wait_timeout"]
+           "dg_selftest_wait_timeout", "dg_quantize_e4m3"]
 
 DG_F32, DG_BF16, DG_E4M3, DG_NVFP4 = 0, 1, 2, 3
 DG_TL_DENOISE, DG_TL_HEAD, DG_TL_MERGE, DG_TL_KERNELS = 0, 1, 2, 3
@@ -122,6 +122,8 @@ def lib():
         L.dg_profile_next_head.restype = C.c_int
         L.dg_profile_next_head_clock.argtypes = [C.c_void_p]
         L.dg_profile_next_head_clock.restype = C.c_int
+        L.dg_quantize_e4m3.argtypes = [vp, C.c_int32, C.c_int32, vp, vp, vp, vp]
+        L.dg_quantize_e4m3.restype = C.c_int
         L.dg_selftest_wait_timeout.argtypes = [C.c_void_p, C.c_void_p]
         L.dg_selftest_wait_timeout.restype = C.c_int
         for f in ("dg_workspace_bytes", "dg_canvas_stats", "dg_canvas_step", "dg_canvas_loop"):
@@ -260,6 +262,19 @@ def dg_nvfp4_pack_scales(block_scales, rows: int, d: int, stream=None) -> torch.
     out = torch.empty(nvfp4_scale_bytes(rows, d), dtype=torch.uint8, device=block_scales.device)
     _check(lib().dg_nvfp4_pack_scales(_ptr(block_scales), int(rows), int(d), _ptr(out),
                                       _stream(stream)), "dg_nvfp4_pack_scales")
+    return out
+
+
+def dg_quantize_e4m3(h, status=None, stream=None) -> dict:
+    """Per-row E4M3 quantisation of bf16 h [rows, d] on the device: codes (uint8 [rows, d]) and
+    row scales (fp32 [rows]), the rule a (BF16, E4M3) pass applies to its hidden states."""
+    rows, d = int(h.shape[0]), int(h.shape[1])
+    dev = h.device
+    out = {"codes": torch.empty(rows, d, dtype=torch.uint8, device=dev),
+           "scale": torch.empty(rows, dtype=torch.float32, device=dev),
+           "status": torch.zeros(1, dtype=torch.int32, device=dev) if status is None else status}
+    _check(lib().dg_quantize_e4m3(_ptr(h), rows, d, _ptr(out["codes"]), _ptr(out["scale"]),
+                                  _ptr(out["status"]), _stream(stream)), "dg_quantize_e4m3")
     return out
 
 

@@ -934,6 +934,17 @@ extern "C" int dg_nvfp4_pack_scales(const uint8_t* block_scales, int32_t rows, i
     return DG_OK;
 }
 
+extern "C" int dg_quantize_e4m3(const void* h_bf16, int32_t rows, int32_t d, uint8_t* codes,
+                                float* row_scale, uint32_t* status, dg_stream_t stream) {
+    dg::NvtxRange nvtx_range("dg_quantize_e4m3");
+    if (!h_bf16 || !codes || !row_scale || rows < 1 || d < 1) return DG_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(h_bf16) & 15u) return DG_ERR_ALIGNMENT;
+    if (dg::launch_quant_rows(static_cast<const uint16_t*>(h_bf16), rows, d, codes, row_scale,
+                              status, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return DG_ERR_CUDA;
+    return DG_OK;
+}
+
 extern "C" int dg_quantize_nvfp4(const void* h_bf16, int32_t rows, int32_t d, uint8_t* codes,
                                  uint8_t* block_scale_packed, float* row_scale, uint32_t* status,
                                  dg_stream_t stream) {
