@@ -238,6 +238,28 @@ def test_loop_e4m3_v32768_lockstep_and_free_run(dg, orc):
     _loop_checks(dg, orc, cfg, x, res)
 
 
+def test_loop_fused_e4m3_quantiser_matches_the_standalone_one(dg, orc):
+    """Inside the FP8 loop the built-in denoiser quantises the hidden states it writes (fused);
+    quantising the traced bf16 hidden states of each pass with dg_quantize_e4m3 and running the
+    same head on them with dg_canvas_stats reproduces that pass's statistics bit for bit, so the
+    fused quantiser and the standalone one (checked code by code against the oracle) agree."""
+    from workloads import WorkloadConfig, make_loop_inputs
+    cfg = WorkloadConfig("loop_e4m3_v32768_d256", "e4m3", 1, 256, 32768, 256, seed=3, mode="loop")
+    x = make_loop_inputs(cfg)
+    res = _run_loop(dg, cfg, x)
+    tw, tws = _head(cfg, x)
+    P = int(dg.state_fields(res["state"])["passes"][0])
+    assert P >= 2
+    for p in range(P):
+        q = dg.dg_quantize_e4m3(res["trace_h"][p].view(torch.bfloat16))
+        st = dg.dg_canvas_stats(q["codes"], tw, B=cfg.B, S=cfg.S, h_scale=q["scale"],
+                                w_scale=tws, h_dtype=dg.DG_E4M3, w_dtype=dg.DG_E4M3)
+        torch.cuda.synchronize()
+        assert torch.equal(st["argmax"], res["trace_argmax"][p]), p
+        assert torch.equal(st["conf"], res["trace_conf"][p]), p
+        assert torch.equal(st["entropy"], res["trace_entropy"][p]), p
+
+
 def test_loop_e4m3_full_scale_lockstep_all_rows(dg, orc):
     """The FP8 loop at 256 slots x 262144 vocab x d=2816 in the launch configuration the
     benchmark times, every pass checked on every row: the denoiser output against the oracle's
