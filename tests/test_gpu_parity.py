@@ -149,6 +149,18 @@ def test_e4m3_prequantised_h_matches_device_quantiser(dg, orc):
         assert torch.equal(a[k], b[k]), k
 
 
+@pytest.mark.parametrize("dtype,inv_temp", [("bf16", 0.5), ("bf16", 1.25), ("e4m3", 2.5),
+                                            ("f32", 0.8)])
+def test_inverse_temperature(dg, orc, dtype, inv_temp):
+    """The descriptor's inv_temp scales every logit before the statistics (l / T with
+    T = 1 / inv_temp): a sharper or flatter softmax, against the oracle at the same scale."""
+    B, S, V, d = 2, 150, 2500, 256 if dtype != "f32" else 64
+    g, o, _ = _run_step(dg, orc, B, S, V, d, dtype, K=40, seed=17, pass_=2, inv_temp=inv_temp)
+    assert int(g["status"][0]) == 0
+    check_stats(g, o, TOL[dtype])
+    check_select(g, o, B, S, V, 40, 17, 2, orc.draw)
+
+
 @pytest.mark.parametrize("B,S,K", [(3, 1, 0), (3, 1, 1), (1, 1024, 500), (2, 513, 100)])
 def test_canvas_size_extremes(dg, orc, B, S, K):
     """One-slot canvases (each a cluster with seven idle CTAs), the largest canvas the merge
