@@ -149,6 +149,22 @@ def test_e4m3_prequantised_h_matches_device_quantiser(dg, orc):
         assert torch.equal(a[k], b[k]), k
 
 
+@pytest.mark.parametrize("dtype,B,S,V,d", [
+    ("bf16", 1, 256, 30000, 256),     # 118 tiles: more than the pairs, one tile per pair
+    ("bf16", 1, 200, 23333, 512),     # 200 rows, ragged vocabulary
+    ("bf16", 1, 256, 37888, 2816),    # 148 tiles, 44 K slices through a 3-stage ring
+    ("e4m3", 1, 256, 30000, 256),
+    ("e4m3", 2, 100, 26000, 2816),
+])
+def test_pair_head_one_or_two_tiles_per_pair(dg, orc, dtype, B, S, V, d):
+    """One 256-row block with more vocabulary tiles than CTA pairs but at most twice as many:
+    some pairs take two tiles (both accumulators of a pair in use), the others one."""
+    g, o, _ = _run_step(dg, orc, B, S, V, d, dtype, K=32, seed=V % 1000, pass_=1)
+    assert int(g["status"][0]) == 0
+    check_stats(g, o, TOL[dtype])
+    check_select(g, o, B, S, V, 32, V % 1000, 1, orc.draw)
+
+
 @pytest.mark.parametrize("dtype,inv_temp", [("bf16", 0.5), ("bf16", 1.25), ("e4m3", 2.5),
                                             ("f32", 0.8)])
 def test_inverse_temperature(dg, orc, dtype, inv_temp):
