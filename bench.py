@@ -213,6 +213,32 @@ def load_peaks():
 
 DATASHEET = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0, "e4m3_tflops": 4500.0}
 
+
+def measure_e4m3_peak(device, n=8192, reps=10):
+    """Dense E4M3 tensor rate of this GPU, measured the way the bf16 peak is: a cuBLAS GEMM
+    (torch._scaled_mm, E4M3 x E4M3 -> bf16, n^3, unit scales), 3 untimed and `reps` timed calls
+    between CUDA events, as a burst. None if the library call is unavailable."""
+    try:
+        g = torch.Generator(device=device).manual_seed(0)
+        a = torch.randn(n, n, device=device, generator=g).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=device, generator=g).to(torch.float8_e4m3fn)
+        one = torch.ones((), device=device, dtype=torch.float32)
+        mm = lambda: torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        for _ in range(3):
+            mm()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            mm()
+        e1.record()
+        torch.cuda.synchronize()
+        s = e0.elapsed_time(e1) / 1e3 / reps
+        del a, b
+        torch.cuda.empty_cache()
+        return 2.0 * n ** 3 / s / 1e12
+    except (RuntimeError, AttributeError, TypeError):
+        return None
+
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the head kernel,
 # from an ncu capture of the build whose head sources hash to `src` (summaries in profiles/).
 # A different hash means the kernel changed since the counters were taken: traffic is null.
@@ -266,6 +292,7 @@ def roofline(cfg, r, peaks, peak_kind, step_s, regime="burst"):
     (8 TB/s, 2.25 PFLOP/s dense bf16) is reported beside it."""
     head_s = statistics.mean(r["head_ms"]) / 1e3
     ratio = {"e4m3": 2.0, "nvfp4": 6.0}.get(cfg.precision, 1.0)
+    e4m3_measured = peaks.get("e4m3_tflops") if cfg.precision == "e4m3" else None
     if regime == "sustained" and cfg.precision != "f32":
         sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * ratio * 1e12
         if r["flops"] / head_s > sus:   # a rate the kernel beats is no ceiling: use the burst one
@@ -275,6 +302,9 @@ def roofline(cfg, r, peaks, peak_kind, step_s, regime="burst"):
     if cfg.precision == "f32":
         tens, tunit = ALU_FP32_FLOP_PER_CLK * 2.032e9 / 1e12, "alu"
         src = "fp32 FMA lanes x maximum SM clock"
+    elif e4m3_measured and regime == "burst":
+        tens, tunit = e4m3_measured, "tensor"
+        src = "E4M3 cuBLAS (torch._scaled_mm 8192^3) measured in this run, burst"
     else:
         tens, tunit = bf16 * ratio, "tensor"
         src = f"{peak_kind} {regime} bf16 cuBLAS" + \
@@ -310,6 +340,8 @@ def roofline(cfg, r, peaks, peak_kind, step_s, regime="burst"):
         out["tensor_frac_burst"] = r["flops"] / head_s / 1e12 / (peaks["bf16_tflops"] * ratio)
         out["tensor_frac_sustained"] = r["flops"] / head_s / 1e12 / (
             peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * ratio)
+        if e4m3_measured:
+            out["tensor_frac_e4m3_measured"] = r["flops"] / head_s / 1e12 / e4m3_measured
         ds_t = max(r["bytes"] / (DATASHEET["hbm_gbs"] * 1e9),
                    r["flops"] / (DATASHEET["bf16_tflops"] * ratio * 1e12))
         out["datasheet_t_roof_us"] = ds_t * 1e6
@@ -733,15 +765,20 @@ def main():
     e2e_steps = max(10, args.steps // 4) if cfg.mode == "pass" else max(3, args.steps // 4)
     with ClockSampler(torch.cuda.current_device()) as clk:
         r = run(cfg, args.steps, args.warmup, ws_, clk, e2e_steps=e2e_steps)
-        extras = {}
+        raw = {}
         if args.workloads == "all" and ws_ == 1:
             for name, (k, w) in EXTRA_WORKLOADS.items():
                 if name == cfg.name:
                     continue
                 c = CONFIGS[name]
-                rr = (run_pass if c.mode == "pass" else run_loop)(c, k, w, 1, clk)
+                raw[name] = (run_pass if c.mode == "pass" else run_loop)(c, k, w, 1, clk)
                 torch.cuda.empty_cache()
-                extras[name] = summarise(c, rr, peaks, peak_kind)
+    # the E4M3 tensor peak, measured after every timed region so that it heats none of them
+    if cfg.precision == "e4m3" or any(CONFIGS[n].precision == "e4m3" for n in raw):
+        e4 = measure_e4m3_peak(torch.device("cuda", local))
+        if e4:
+            peaks = {**peaks, "e4m3_tflops": e4}
+    extras = {name: summarise(CONFIGS[name], rr, peaks, peak_kind) for name, rr in raw.items()}
     t_max = max_over_ranks(r["t_s"], ws_, torch.device("cuda", local))
     e_max = max_over_ranks(r["e2e_t_s"], ws_, torch.device("cuda", local))
     if rank != 0:
@@ -761,7 +798,10 @@ def main():
             "gpu_launches": r["launches"], "clocks": r["clocks"], "device_status": r["status"],
             "peaks": {"source": peak_kind, **{k: peaks[k] for k in ("hbm_gbs", "bf16_tflops")
                                               if k in peaks},
-                      "bf16_tflops_sustained": peaks.get("bf16_tflops_sustained")}}
+                      "bf16_tflops_sustained": peaks.get("bf16_tflops_sustained"),
+                      "e4m3_tflops": peaks.get("e4m3_tflops"),
+                      "e4m3_source": ("torch._scaled_mm 8192^3, burst, measured in this run"
+                                      if peaks.get("e4m3_tflops") else "2 x bf16 (nominal ratio)")}}
     if r.get("head_ms"):
         step_s = t_max / (r["units"] / cfg.B)
         line["roofline"] = roofline(cfg, r, peaks, peak_kind, step_s,

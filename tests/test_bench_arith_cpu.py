@@ -153,3 +153,24 @@ def test_loop_breakdown_from_a_timeline():
     assert out["gap_next_pass"] == 4.0
     assert out["per_pass"] == 22.0
     assert not math.isnan(out["per_pass"])
+
+
+def test_e4m3_roofline_uses_the_measured_e4m3_peak_when_there_is_one():
+    """With an E4M3 GEMM rate measured in the run, the FP8 head's tensor term uses it (burst
+    regime) instead of twice the bf16 rate; a measured rate below 2 x bf16 can make the head
+    tensor-bound where the nominal ratio had it HBM-bound."""
+    cfg = CONFIGS["loop_e4m3_v262144_d2816"]
+    flops, byts = bench.algorithmic(cfg)
+    r = {"head_ms": [0.150], "flops": flops, "bytes": byts}
+    nominal = bench.roofline(cfg, r, PEAKS, "measured", step_s=160e-6)
+    measured = bench.roofline(cfg, r, {**PEAKS, "e4m3_tflops": 3000.0}, "measured", step_s=160e-6)
+    # t_flop = 3.78e11 / 3.0e15 = 126 us > t_mem = 0.74e9 / 6.5e12 = 114 us: tensor-bound
+    assert measured["bound"] == "tensor" and measured["peak"] == 3000.0
+    assert measured["frac"] == pytest.approx(flops / 150e-6 / 3.0e15)
+    assert "measured in this run" in measured["peak_source"]
+    assert measured["tensor_frac_e4m3_measured"] == pytest.approx(flops / 150e-6 / 3.0e15)
+    assert nominal["bound"] == "hbm"
+    # the sustained regime keeps the nominal ratio (no sustained E4M3 measurement)
+    sus = bench.roofline(cfg, r, {**PEAKS, "e4m3_tflops": 3000.0}, "measured", step_s=160e-6,
+                         regime="sustained")
+    assert "x2 nominal" in sus.get("peak_source", "") or sus["bound"] == "hbm"
