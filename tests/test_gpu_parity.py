@@ -165,6 +165,20 @@ def test_pair_head_one_or_two_tiles_per_pair(dg, orc, dtype, B, S, V, d):
     check_select(g, o, B, S, V, 32, V % 1000, 1, orc.draw)
 
 
+@pytest.mark.parametrize("dtype,V,d", [(dt, V, d) for dt, ds in (("bf16", (8, 16)),
+                                                                    ("f32", (4, 8, 16)),
+                                                                    ("e4m3", (16,)))
+                                         for V in (17, 33, 4097) for d in ds])
+def test_tiny_heads(dg, orc, dtype, V, d):
+    """The smallest hidden sizes each precision allows (one 16-byte row) and vocabularies just
+    past a power of two: one K slice mostly zero-filled, one partial tile."""
+    B, S = 2, 130
+    g, o, _ = _run_step(dg, orc, B, S, V, d, dtype, K=9, seed=V * d, pass_=4)
+    assert int(g["status"][0]) == 0
+    check_stats(g, o, TOL[dtype])
+    check_select(g, o, B, S, V, 9, V * d, 4, orc.draw)
+
+
 @pytest.mark.parametrize("dtype,inv_temp", [("bf16", 0.5), ("bf16", 1.25), ("e4m3", 2.5),
                                             ("f32", 0.8)])
 def test_inverse_temperature(dg, orc, dtype, inv_temp):
