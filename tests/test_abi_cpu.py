@@ -138,6 +138,15 @@ def test_selftest_rejects_null_status(dg):
     assert dg.lib().dg_selftest_wait_timeout(None, None) == -1
 
 
+def test_quantise_e4m3_argument_checks(dg):
+    L = dg.lib()
+    assert L.dg_quantize_e4m3(None, 4, 16, 16, 16, None, None) == -1      # no input
+    assert L.dg_quantize_e4m3(16, 4, 16, None, 16, None, None) == -1      # no codes
+    assert L.dg_quantize_e4m3(16, 0, 16, 16, 16, None, None) == -1        # no rows
+    assert L.dg_quantize_e4m3(16, 4, 0, 16, 16, None, None) == -1         # no width
+    assert L.dg_quantize_e4m3(17, 4, 16, 16, 16, None, None) == -2        # misaligned input
+
+
 def test_status_strings(dg):
     for code in (0, -1, -2, -3, -4, -5, 1, 2, 4):
         s = dg.dg_status_string(code)
