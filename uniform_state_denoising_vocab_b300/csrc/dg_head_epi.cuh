@@ -32,8 +32,12 @@ __device__ __forceinline__ void drain_tile(RowState& st, uint32_t taddr0, const 
         __syncwarp();
         tmem_ld32(taddr0 + c * 32, v);
         if (KIND == 1) {
+            const float2* c2 = reinterpret_cast<const float2*>(csc + c * 32);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] *= csc[c * 32 + j];
+            for (int j = 0; j < 16; ++j) {
+                const float2 sc = c2[j];
+                mul_x2(v[2 * j], v[2 * j + 1], v[2 * j], v[2 * j + 1], sc.x, sc.y);
+            }
         }
         const int valid = valid_tile - c * 32;
         if (valid >= 32)
@@ -52,8 +56,12 @@ __device__ __forceinline__ void fold_columns(RowState& st, float (&v)[NCOL], con
     for (int c = 0; c < NCOL / 32; ++c) {
         float(&w)[32] = *reinterpret_cast<float(*)[32]>(v + c * 32);
         if (KIND == 1) {
+            const float2* c2 = reinterpret_cast<const float2*>(csc + c * 32);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) w[j] *= csc[c * 32 + j];
+            for (int j = 0; j < 16; ++j) {
+                const float2 sc = c2[j];
+                mul_x2(w[2 * j], w[2 * j + 1], w[2 * j], w[2 * j + 1], sc.x, sc.y);
+            }
         }
         const int valid = valid_tile - c * 32;
         if (valid >= 32)
