@@ -247,9 +247,9 @@ HEAD_SOURCES = {
     "fp4": ["dg_head_fp4.cu", "dg_head_epi.cuh", "dg_common.cuh", "dg_ptx.cuh", "dg_internal.h"],
 }
 TRAFFIC = {
-    "pass_bf16_v262144_d2816": {"bytes": 1.477904e9 + 2.641152e6, "src": "a5bd0bde0a2ae050"},
-    "loop_e4m3_v262144_d2816": {"bytes": 740.020992e6 + 3.045888e6, "src": "a5bd0bde0a2ae050"},
-    "pass_nvfp4_v262144_d2816": {"bytes": 417.332992e6 + 3.860992e6, "src": "042ac63692f71b89"},
+    "pass_bf16_v262144_d2816": {"bytes": 1.477882752e9 + 1.546624e6, "src": "c118b87f934b035b"},
+    "loop_e4m3_v262144_d2816": {"bytes": 740.019712e6 + 1.556864e6, "src": "c118b87f934b035b"},
+    "pass_nvfp4_v262144_d2816": {"bytes": 417.154944e6 + 2.19584e6, "src": "5a2dd153528e1ca7"},
 }
 
 
